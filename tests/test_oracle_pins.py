@@ -1,0 +1,573 @@
+"""Pins of the CPU oracle to facts fixed outside it.
+
+Each test checks an oracle function against something other than itself: a
+hand-derived fixture (tests/golden), a closed form, an invariant of the
+mathematics, a library routine (scipy's Hadamard matrix, torch's float8 and
+bfloat16 casts) or brute force.  They run on the CPU only.
+
+Sources: vLLM page "kpool_compress" (pooled path), sglang page
+"deepseek_v4/c128_online.cuh" (online c128 path and its plan).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bf16_bits(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _bf16_round(x):
+    return _bf16_bits(x).astype(np.uint32).__lshift__(16).view(np.float32)
+
+
+# --------------------------------------------------------------------- formats
+def test_bf16_matches_torch_cast_on_fp32(ora):
+    rng = np.random.default_rng(0)
+    vals = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * np.float32(10.0) ** rng.integers(-30, 30, 20000).astype(np.float32),
+        # exact ties between two bf16 neighbours (low 16 bits = 0x8000)
+        (rng.integers(0x0080, 0x7F00, 2000, dtype=np.uint32) << 16 | 0x8000).view(np.float32),
+        np.array([0.0, -0.0, 1e-40, -1e-40, 3.0e38, 1.17e-38], np.float32),
+    ])
+    vals = vals[np.isfinite(vals)]
+    ref = _bf16_bits(vals)
+    got = np.array([ora.bf16_from_double(float(v)) for v in vals], np.uint16)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_bf16_from_double_is_nearest(ora):
+    # brute force: the result is the closest bf16 value, ties to an even mantissa
+    allb = np.arange(0, 0x7F80, dtype=np.uint32)
+    allv = (allb << 16).view(np.float32).astype(np.float64)
+    rng = np.random.default_rng(1)
+    xs = rng.uniform(-4, 4, 3000)
+    for x in xs:
+        h = ora.bf16_from_double(x)
+        a = abs(x)
+        i = np.searchsorted(allv, a)
+        cand = [j for j in (i - 1, i) if 0 <= j < len(allv)]
+        dist = [abs(allv[j] - a) for j in cand]
+        best = [cand[k] for k in range(len(cand)) if dist[k] == min(dist)]
+        if len(best) > 1:
+            best = [j for j in best if j % 2 == 0]
+        assert (h & 0x7FFF) == best[0]
+        assert (h >> 15) == (1 if x < 0 else 0)
+
+
+def _e4m3_table(ora):
+    codes = np.arange(256)
+    vals = np.array([ora.e4m3_decode(int(c)) for c in codes])
+    return codes, vals
+
+
+def test_e4m3_decode_known_points(ora):
+    # OCP E4M3: max 448 at 0x7E, min normal 2^-6 at 0x08, min subnormal 2^-9 at 0x01, NaN at 0x7F
+    assert ora.e4m3_decode(0x7E) == 448.0
+    assert ora.e4m3_decode(0xFE) == -448.0
+    assert ora.e4m3_decode(0x08) == 2.0 ** -6
+    assert ora.e4m3_decode(0x01) == 2.0 ** -9
+    assert ora.e4m3_decode(0x07) == 7 * 2.0 ** -9
+    assert ora.e4m3_decode(0x38) == 1.0
+    assert math.isnan(ora.e4m3_decode(0x7F))
+    vals = np.array([ora.e4m3_decode(c) for c in range(256)])
+    torch_vals = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    np.testing.assert_array_equal(np.nan_to_num(vals, nan=1e9), np.nan_to_num(torch_vals, nan=1e9))
+
+
+def test_e4m3_encode_exhaustive_bf16_vs_brute_force(ora):
+    codes, vals = _e4m3_table(ora)
+    finite = ~np.isnan(vals)
+    fcodes, fvals = codes[finite], vals[finite]
+    xs = (np.arange(0, 65536, dtype=np.uint32) << 16).view(np.float32)
+    xs = xs[np.isfinite(xs)]
+    for x in xs:
+        c = ora.e4m3_encode(float(x))
+        a = min(abs(float(x)), 448.0)  # saturation
+        pos = fvals >= 0
+        cand_codes = fcodes[pos & ((fcodes & 0x80) == 0)]
+        cand_vals = fvals[pos & ((fcodes & 0x80) == 0)]
+        d = np.abs(cand_vals - a)
+        best = cand_codes[d == d.min()]
+        if len(best) > 1:
+            best = best[best % 2 == 0]
+        assert (c & 0x7F) == int(best[0]), (x, c, best)
+        if c & 0x7F:
+            assert (c >> 7) == (1 if x < 0 else 0)
+
+
+def test_e4m3_round_trip_and_torch_cast(ora):
+    for c in range(256):
+        v = ora.e4m3_decode(c)
+        if math.isnan(v):
+            continue
+        assert ora.e4m3_encode(v) == c
+    rng = np.random.default_rng(2)
+    xs = np.concatenate([rng.uniform(-448, 448, 20000), rng.uniform(-1, 1, 20000) * 2.0 ** -6]).astype(np.float32)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([ora.e4m3_encode(float(x)) for x in xs], np.uint8)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_pow2_ceil(ora):
+    for e in range(-30, 30):
+        assert ora.pow2_ceil(2.0 ** e) == 2.0 ** e
+    rng = np.random.default_rng(3)
+    for v in rng.uniform(1e-7, 10.0, 2000).astype(np.float32):
+        r = ora.pow2_ceil(float(v))
+        m, ex = math.frexp(r)
+        assert m == 0.5  # a power of two
+        assert r / 2 < v <= r
+
+
+# -------------------------------------------------------------------- Hadamard
+def test_hadamard_exact_matches_scipy(ora):
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    H = scipy_linalg.hadamard(128).astype(np.float64) / math.sqrt(128.0)
+    rng = np.random.default_rng(4)
+    for _ in range(20):
+        x = rng.standard_normal(128)
+        np.testing.assert_allclose(ora.hadamard128_exact(x), H @ x, rtol=0, atol=1e-12)
+
+
+def test_hadamard_exact_closed_forms(ora):
+    c = 1.0 / math.sqrt(128.0)
+    e0 = np.zeros(128)
+    e0[0] = 1.0
+    np.testing.assert_allclose(ora.hadamard128_exact(e0), np.full(128, c), atol=1e-15)
+    ones = np.ones(128)
+    np.testing.assert_allclose(ora.hadamard128_exact(ones), math.sqrt(128.0) * e0, atol=1e-12)
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal(128)
+    y = ora.hadamard128_exact(x)
+    np.testing.assert_allclose(ora.hadamard128_exact(y), x, atol=1e-12)  # involution
+    assert abs(np.linalg.norm(y) - np.linalg.norm(x)) < 1e-12          # Parseval
+    # row 5 of the Sylvester matrix: signs (-1)^popcount(5 & j)
+    e5 = np.zeros(128)
+    e5[5] = 1.0
+    col = ora.hadamard128_exact(e5)
+    expect = np.array([(-1) ** bin(5 & j).count("1") for j in range(128)]) * c
+    np.testing.assert_allclose(col, expect, atol=1e-15)
+
+
+def test_hadamard_fp32_butterfly_vs_exact(ora):
+    rng = np.random.default_rng(6)
+    for _ in range(200):
+        x = _bf16_round(rng.standard_normal(128).astype(np.float32) * 0.3)
+        y32 = ora.hadamard128_fp32(x).astype(np.float64)
+        ye = ora.hadamard128_exact(x.astype(np.float64))
+        assert np.max(np.abs(y32 - ye)) <= 1e-6 * max(1.0, np.max(np.abs(ye)))
+        back = ora.hadamard128_fp32(y32.astype(np.float32)).astype(np.float64)
+        assert np.max(np.abs(back - x)) <= 2e-6 * max(1.0, np.max(np.abs(x)))
+
+
+# ------------------------------------------------------------------- quantise
+def test_quantize_scale_invariants(ora):
+    rng = np.random.default_rng(7)
+    for round_scale in (True, False):
+        for _ in range(200):
+            y = _bf16_round(rng.standard_normal(128).astype(np.float32) * rng.uniform(0.01, 30))
+            yb = _bf16_bits(y)
+            q, sc = ora.quantize_rows(yb, round_scale)
+            absmax = max(np.max(np.abs(y)), np.float32(1e-4))
+            dec = np.array([ora.e4m3_decode(int(c)) for c in q])
+            if round_scale:
+                m, _ = math.frexp(float(sc))
+                assert m == 0.5
+                assert 224.0 < absmax / sc <= 448.0 * (1 + 1e-6)
+            else:
+                assert abs(sc - absmax / 448.0) <= 1e-6 * sc
+                assert np.max(np.abs(dec)) == 448.0
+            # every code is the nearest e4m3 value to y/scale (within half a quantum)
+            t = np.clip(y / sc, -448, 448)
+            quantum = np.where(np.abs(t) < 2 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(np.abs(t), 1e-30))) - 3))
+            assert np.all(np.abs(dec - t) <= quantum / 2 * (1 + 1e-6))
+
+
+def test_quantize_floor_on_zero_row(ora):
+    q, sc = ora.quantize_rows(np.zeros(128, np.uint16), True)
+    assert sc == ora.pow2_ceil(np.float32(1e-4) * np.float32(1.0 / 448.0))
+    assert np.all(q == 0)
+
+
+# --------------------------------------------------------------- pool softmax
+def _pool(ora, k, s, ape, rs=True):
+    return ora.pool_compress(k, s, ape, rs)
+
+
+@pytest.mark.parametrize("case", json.load(open(os.path.join(GOLDEN, "pool_examples.json")))["cases"],
+                         ids=lambda c: c["name"])
+def test_pool_golden(ora, case):
+    P = case["P"]
+    k = np.repeat(np.array(case["keys"], np.float32)[:, None], 128, 1)
+    s = np.repeat(np.array(case["scores"], np.float32)[:, None], 128, 1)
+    ape = np.repeat(np.array(case["ape"], np.float32)[:, None], 128, 1)
+    r = _pool(ora, k, s, ape, True)
+    np.testing.assert_allclose(r["x"], case["x"], rtol=0, atol=1e-6)
+    assert np.all(r["xb"] == case["xb"])
+    if "yb0" in case:
+        assert r["yb"][0] == case["yb0"] and np.all(r["yb"][1:] == 0)
+        assert r["scale"] == case["round"]["scale"] and r["q"][0] == case["round"]["q0"]
+        assert np.all(r["q"][1:] == 0)
+        r2 = _pool(ora, k, s, ape, False)
+        absmax = ora.bf16_to_float(case["yb0"]) if hasattr(ora, "bf16_to_float") else 28.25
+        assert abs(r2["scale"] - 28.25 * case["linear"]["scale_over_absmax"]) < 1e-8
+        assert r2["q"][0] == case["linear"]["q0"]
+
+
+def test_pool_equal_scores_give_mean(ora):
+    rng = np.random.default_rng(8)
+    for P in (1, 2, 4, 8, 16):
+        k = _bf16_round(rng.standard_normal((P, 128)).astype(np.float32))
+        s = np.repeat(rng.standard_normal((1, 128)).astype(np.float32), P, 0)
+        ape = np.repeat(rng.standard_normal((1, 128)).astype(np.float32) * 0.1, P, 0)
+        r = _pool(ora, k, s, ape)
+        np.testing.assert_allclose(r["x"], k.astype(np.float64).mean(0), atol=1e-12)
+
+
+def test_pool_dominant_score_and_bias(ora):
+    rng = np.random.default_rng(9)
+    for P in (2, 4, 16):
+        for jstar in (0, P // 2, P - 1):
+            k = _bf16_round(rng.standard_normal((P, 128)).astype(np.float32))
+            s = rng.standard_normal((P, 128)).astype(np.float32)
+            s[jstar] += 60.0
+            ape = (rng.standard_normal((P, 128)) * 0.1).astype(np.float32)
+            r = _pool(ora, k, s, ape)
+            np.testing.assert_allclose(r["x"], k[jstar], atol=1e-12)
+            # same selection made by the position bias alone (catches a wrong ape row)
+            s2 = np.zeros((P, 128), np.float32)
+            ape2 = np.zeros((P, 128), np.float32)
+            ape2[jstar] = 60.0
+            r2 = _pool(ora, k, s2, ape2)
+            np.testing.assert_allclose(r2["x"], k[jstar], atol=1e-12)
+
+
+def test_pool_p1_identity(ora):
+    rng = np.random.default_rng(10)
+    k = _bf16_round(rng.standard_normal((1, 128)).astype(np.float32))
+    r = _pool(ora, k, rng.standard_normal((1, 128)).astype(np.float32), np.zeros((1, 128), np.float32))
+    np.testing.assert_array_equal(r["x"], k[0].astype(np.float64))
+    np.testing.assert_array_equal(r["xb"], _bf16_bits(k[0]))
+
+
+def test_pool_two_slot_logistic_closed_form(ora):
+    # P=2: x = k0 * sigma(z0 - z1) + k1 * sigma(z1 - z0), sigma the logistic function
+    rng = np.random.default_rng(11)
+    k = rng.standard_normal((2, 128)).astype(np.float32)
+    s = (rng.standard_normal((2, 128)) * 3).astype(np.float32)
+    ape = (rng.standard_normal((2, 128)) * 0.1).astype(np.float32)
+    z = s.astype(np.float64) + ape
+    sig = 1.0 / (1.0 + np.exp(-(z[0] - z[1])))
+    expect = k[0] * sig + k[1] * (1.0 - sig)
+    np.testing.assert_allclose(_pool(ora, k, s, ape)["x"], expect, atol=1e-12)
+
+
+def test_pool_brute_force_small_chunks(ora):
+    # every assignment of keys and scores from {-1, 0, 1} for P <= 3 (one per channel),
+    # plus permutation / shift / affine invariances and convexity.
+    import itertools
+
+    for P in (2, 3):
+        combos = list(itertools.product((-1.0, 0.0, 1.0), repeat=2 * P))
+        for start in range(0, len(combos), 128):
+            chunk = combos[start:start + 128]
+            chunk = chunk + [chunk[-1]] * (128 - len(chunk))
+            arr = np.array(chunk, np.float32).T  # [2P, 128]
+            k, s = arr[:P], arr[P:]
+            ape = np.zeros((P, 128), np.float32)
+            x = _pool(ora, k, s, ape)["x"]
+            # closed form without the max shift: weights e^{s_j} / sum e^{s_i}
+            w = np.exp(s.astype(np.float64))
+            expect = (w * k).sum(0) / w.sum(0)
+            np.testing.assert_allclose(x, expect, atol=1e-14)
+    rng = np.random.default_rng(12)
+    P = 16
+    # bf16-valued inputs so that the shifted / scaled copies below are exact in fp32
+    k = _bf16_round(rng.standard_normal((P, 128)).astype(np.float32))
+    s = _bf16_round((rng.standard_normal((P, 128)) * 2).astype(np.float32))
+    ape = _bf16_round((rng.standard_normal((P, 128)) * 0.1).astype(np.float32))
+    x = _pool(ora, k, s, ape)["x"]
+    perm = rng.permutation(P)
+    np.testing.assert_allclose(_pool(ora, k[perm], s[perm], ape[perm])["x"], x, atol=1e-12)
+    np.testing.assert_allclose(_pool(ora, k, s, ape + np.float32(3.0))["x"], x, atol=1e-12)
+    np.testing.assert_allclose(_pool(ora, 2 * k + 1, s, ape)["x"], 2 * x + 1, atol=1e-12)
+    assert np.all(x <= k.max(0) + 1e-12) and np.all(x >= k.min(0) - 1e-12)
+
+
+# ------------------------------------------------------------ pooled kernels
+def _rand_bf16(rng, shape, scale=1.0):
+    return _bf16_bits((rng.standard_normal(shape) * scale).astype(np.float32))
+
+
+def test_kpool_compress_cache_layout(ora):
+    # one pool written at loc: the FP8 row sits at page*ps*(D+4) + tok*D, the fp32 scale
+    # at byte page*ps*(D+4) + ps*D + 4*tok; nothing else changes.
+    rng = np.random.default_rng(13)
+    P, D, ps, pages = 16, 128, 64, 3
+    k = _rand_bf16(rng, (1, P, D))
+    s = _rand_bf16(rng, (1, P, D))
+    ape = (rng.standard_normal((P, D)) * 0.1).astype(np.float32)
+    for loc in (0, 63, 64, 130):
+        cache = np.full((pages, ps, D + 4), 0xAB, np.uint8)
+        r = ora.kpool_compress(cache, ps, k, s, ape, np.array([loc]), return_compressed=True)
+        flat = cache.reshape(-1)
+        page, tok = divmod(loc, ps)
+        row0 = page * ps * (D + 4) + tok * D
+        sc0 = page * ps * (D + 4) + ps * D + 4 * tok
+        np.testing.assert_array_equal(flat[row0:row0 + D], r["q"][0])
+        assert flat[sc0:sc0 + 4].view(np.float32)[0] == r["scale"][0]
+        mask = np.ones(flat.size, bool)
+        mask[row0:row0 + D] = False
+        mask[sc0:sc0 + 4] = False
+        assert np.all(flat[mask] == 0xAB)
+
+
+def test_kpool_compress_write_mask(ora):
+    rng = np.random.default_rng(14)
+    P, D, ps = 16, 128, 64
+    n = 8
+    k = _rand_bf16(rng, (n, P, D))
+    s = _rand_bf16(rng, (n, P, D))
+    ape = (rng.standard_normal((P, D)) * 0.1).astype(np.float32)
+    loc = np.arange(n, dtype=np.int64)
+    wm = np.array([1, 0, 1, 1, 0, 0, 1, 0], np.uint8)
+    c1 = np.zeros((1, ps, D + 4), np.uint8)
+    ora.kpool_compress(c1, ps, k, s, ape, loc, write_mask=wm)
+    c2 = np.zeros((1, ps, D + 4), np.uint8)
+    ora.kpool_compress(c2, ps, k[wm == 1], s[wm == 1], ape, loc[wm == 1])
+    np.testing.assert_array_equal(c1, c2)
+
+
+def _decode_case(rng, B, positions_start, N, P=16, D=128, ring_blocks=None):
+    ring_blocks = ring_blocks or B
+    blocks = rng.permutation(ring_blocks)[:B]
+    pos = positions_start[:, None] + np.arange(N)[None, :]
+    tslot = (blocks[:, None] * P + pos % P).astype(np.int32)
+    loc = np.where(pos % P == P - 1, np.arange(B)[:, None] * 4096 + pos // P, -1).astype(np.int32)
+    return blocks, pos.astype(np.int32), tslot, loc
+
+
+def test_kpool_decode_matches_one_shot_from_empty_ring(ora):
+    # N = 64 tokens from position 0 per request: 4 pools each, all built in one call
+    rng = np.random.default_rng(15)
+    B, N, P, D, ps = 4, 64, 16, 128, 64
+    blocks, pos, tslot, loc = _decode_case(rng, B, np.zeros(B, np.int64), N)
+    loc = np.where(pos % P == P - 1, np.arange(B)[:, None] * 4 + pos // P, -1).astype(np.int32)
+    key = _rand_bf16(rng, (B, N, D))
+    score = _rand_bf16(rng, (B, N, D))
+    ape = _bf16_round((rng.standard_normal((P, D)) * 0.1).astype(np.float32))
+    ring = np.zeros((B, 2, P, D), np.uint16)
+    cache = np.zeros((1, ps, D + 4), np.uint8)
+    ora.kpool_decode_update(cache, ps, ring, tslot, loc, pos, key, score, ape)
+    cache2 = np.zeros_like(cache)
+    slot_k = key.reshape(B * 4, P, D)
+    slot_s = score.reshape(B * 4, P, D)
+    ora.kpool_compress(cache2, ps, slot_k, slot_s, ape, np.arange(B * 4, dtype=np.int64))
+    np.testing.assert_array_equal(cache, cache2)
+    # the ring now holds each request's last pool, slot by slot
+    for b in range(B):
+        np.testing.assert_array_equal(ring[blocks[b], 0], key[b, -P:])
+        np.testing.assert_array_equal(ring[blocks[b], 1], score[b, -P:])
+
+
+def test_kpool_decode_pool_across_calls_uses_fresh_stashes(ora):
+    # a pool filled over three calls must compress the stashed tokens of those calls,
+    # not stale ring contents (ordering/gating regression named on the kpool page)
+    rng = np.random.default_rng(16)
+    P, D, ps = 16, 128, 64
+    key = _rand_bf16(rng, (1, P, D))
+    score = _rand_bf16(rng, (1, P, D))
+    ape = (rng.standard_normal((P, D)) * 0.1).astype(np.float32)
+    ring = _rand_bf16(rng, (2, 2, P, D))  # stale garbage
+    cache = np.zeros((1, ps, D + 4), np.uint8)
+    for lo, hi in ((0, 6), (6, 11), (11, 16)):
+        pos = np.arange(lo, hi, dtype=np.int32)[None, :]
+        tslot = (1 * P + pos % P).astype(np.int32)
+        loc = np.where(pos % P == P - 1, 5, -1).astype(np.int32)
+        ora.kpool_decode_update(cache, ps, ring, tslot, loc, pos, key[:, lo:hi], score[:, lo:hi], ape)
+    ref = ora.pool_compress(_bf16_round_bits(key[0]), _bf16_round_bits(score[0]), ape, True)
+    flat = cache.reshape(-1)  # linear page layout: rows at tok*D, scales after ps*D bytes
+    np.testing.assert_array_equal(flat[5 * D:6 * D], ref["q"])
+    assert flat[ps * D + 20:ps * D + 24].view(np.float32)[0] == ref["scale"]
+
+
+def _bf16_round_bits(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def test_kpool_decode_padding_is_inert(ora):
+    rng = np.random.default_rng(17)
+    B, N, P, D, ps = 3, 4, 16, 128, 64
+    ring = _rand_bf16(rng, (B, 2, P, D))
+    ring0 = ring.copy()
+    cache = np.zeros((1, ps, D + 4), np.uint8)
+    neg = -np.ones((B, N), np.int32)
+    ora.kpool_decode_update(cache, ps, ring, neg, neg, neg, _rand_bf16(rng, (B, N, D)),
+                            _rand_bf16(rng, (B, N, D)), np.zeros((P, D), np.float32))
+    np.testing.assert_array_equal(ring, ring0)
+    assert np.all(cache == 0)
+
+
+def test_kpool_seed_tail_selects_last_pool(ora):
+    # two requests of 21 and 7 prefill tokens; request r's tail block is r; a token is
+    # seeded iff it is among its request's last P tokens
+    rng = np.random.default_rng(18)
+    P, D = 16, 128
+    lens = [21, 7]
+    tslot = np.concatenate([r * P + np.arange(n) % P for r, n in enumerate(lens)]).astype(np.int32)
+    n = len(tslot)
+    key = _rand_bf16(rng, (n, D))
+    score = _rand_bf16(rng, (n, D))
+    ring = np.zeros((2, 2, P, D), np.uint16)
+    ora.kpool_seed_tail(ring, key, score, tslot)
+    seeded = np.zeros((2, P), bool)
+    for i in range(n):
+        r = 0 if i < lens[0] else 1
+        idx_in_req = i if r == 0 else i - lens[0]
+        if idx_in_req >= lens[r] - P:
+            np.testing.assert_array_equal(ring[r, 0, tslot[i] % P], key[i])
+            np.testing.assert_array_equal(ring[r, 1, tslot[i] % P], score[i])
+            seeded[r, tslot[i] % P] = True
+    assert np.all(ring[0][:, ~seeded[0]] == 0) and np.all(ring[1][:, ~seeded[1]] == 0)
+
+
+# ---------------------------------------------------------------- online c128
+def test_c128_golden_two_tokens(ora):
+    case = json.load(open(os.path.join(GOLDEN, "c128_examples.json")))["cases"][0]
+    D = 128
+    state = np.zeros((1, 3, D), np.float32)
+    ape = np.zeros((128, D), np.float32)
+    for t, (kk, ss) in enumerate(zip(case["keys"], case["scores"])):
+        inp = np.concatenate([np.full(D, kk, np.float32), np.full(D, ss, np.float32)])[None]
+        out, ns, closed = ora.c128_decode(state, inp, ape, np.array([0]), np.array([t + 1]))
+        np.testing.assert_allclose(ns[0, :, 0], case["state_after"][t], rtol=1e-6, atol=1e-6)
+        state[0] = ns[0].astype(np.float32)
+
+
+def test_c128_decode_chunk_equals_two_pass(ora):
+    # 128 single-token updates from chunk position 0 == a two-pass softmax over the chunk
+    rng = np.random.default_rng(19)
+    D = 256
+    k = rng.standard_normal((128, D)).astype(np.float32)
+    s = (rng.standard_normal((128, D)) * 2).astype(np.float32)
+    ape = (rng.standard_normal((128, D)) * 0.1).astype(np.float32)
+    state = np.zeros((1, 3, D), np.float32)
+    seq0 = 128 * 7  # chunk starts at seq_len-1 = 896
+    for t in range(128):
+        inp = np.concatenate([k[t], s[t]])[None]
+        out, ns, closed = ora.c128_decode(state, inp, ape, np.array([0]), np.array([seq0 + t + 1]))
+        assert closed[0] == (t == 127)
+        if t == 0:
+            np.testing.assert_array_equal(ns[0, 1], 1.0)
+            np.testing.assert_array_equal(ns[0, 2], k[0])
+        if t < 127:
+            state[0] = ns[0]
+    z = s.astype(np.float64) + ape
+    w = np.exp(z - z.max(0))
+    ref = (w * k).sum(0) / w.sum(0)
+    np.testing.assert_allclose(out[0], ref, rtol=2e-6, atol=2e-6)
+    # and the oracle's own prefill path (two-pass over the chunk) agrees
+    inp_all = np.concatenate([k, s], 1)
+    pout, written, fs, sw = ora.c128_prefill(np.zeros((1, 3, D), np.float32), inp_all, ape,
+                                             np.array([0]), np.array([seq0 + 128]), np.array([128]))
+    assert written[127] and written.sum() == 1 and not sw[0]
+    np.testing.assert_allclose(pout[127], out[0], rtol=2e-6, atol=2e-6)
+
+
+def test_c128_decode_position_from_seq_len_minus_one(ora):
+    # seq_len % 128 == 0 means the token sits at chunk position 127 and closes the chunk;
+    # seq_len % 128 == 1 means position 0 and starts a new chunk from this token alone
+    D = 128
+    rng = np.random.default_rng(20)
+    state = rng.standard_normal((2, 3, D)).astype(np.float32)
+    state[:, 1] = np.abs(state[:, 1]) + 1
+    inp = rng.standard_normal((2, 2 * D)).astype(np.float32)
+    ape = (rng.standard_normal((128, D)) * 0.1).astype(np.float32)
+    out, ns, closed = ora.c128_decode(state, inp, ape, np.array([0, 1]), np.array([256, 257]))
+    assert closed[0] and not closed[1]
+    np.testing.assert_array_equal(ns[1, 0], inp[1, D:].astype(np.float64) + ape[0])
+    np.testing.assert_array_equal(ns[1, 2], inp[1, :D])
+
+
+def test_c128_prefill_split_equals_whole(ora):
+    # prefill of a request in several extend pieces, chaining the partial state through the
+    # slot, equals a single extend (checkpoint/resume of the running state)
+    rng = np.random.default_rng(21)
+    D = 128
+    T = 700
+    prefix = 37
+    k = rng.standard_normal((T, D)).astype(np.float32)
+    s = (rng.standard_normal((T, D)) * 2).astype(np.float32)
+    ape = (rng.standard_normal((128, D)) * 0.1).astype(np.float32)
+    inp = np.concatenate([k, s], 1)
+    # prior partial state for positions [0, 37) built by the oracle from virtual tokens
+    pk = rng.standard_normal((prefix, D)).astype(np.float32)
+    psc = rng.standard_normal((prefix, D)).astype(np.float32)
+    _, _, fs0, sw0 = ora.c128_prefill(np.zeros((1, 3, D), np.float32), np.concatenate([pk, psc], 1), ape,
+                                      np.array([0]), np.array([prefix]), np.array([prefix]))
+    st0 = fs0.astype(np.float32)
+    whole_out, whole_w, whole_fs, _ = ora.c128_prefill(st0, inp, ape, np.array([0]),
+                                                       np.array([prefix + T]), np.array([T]))
+    cuts = [0, 1, 91, 92, 219, 500, 640, T]
+    st = st0.copy()
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        o, w, fs, sw = ora.c128_prefill(st, inp[a:b], ape, np.array([0]), np.array([prefix + b]),
+                                        np.array([b - a]))
+        for r in np.nonzero(w)[0]:
+            assert whole_w[a + r]
+            np.testing.assert_allclose(o[r], whole_out[a + r], rtol=1e-5, atol=1e-5)
+        if sw[0]:
+            st = fs.astype(np.float32)
+    np.testing.assert_allclose(st[0], whole_fs[0], rtol=1e-5, atol=1e-5)
+
+
+def test_c128_prefill_single_token_window(ora):
+    D = 128
+    rng = np.random.default_rng(22)
+    inp = rng.standard_normal((1, 2 * D)).astype(np.float32)
+    ape = (rng.standard_normal((128, D)) * 0.1).astype(np.float32)
+    _, w, fs, sw = ora.c128_prefill(np.zeros((1, 3, D), np.float32), inp, ape, np.array([0]),
+                                    np.array([129]), np.array([1]))
+    assert sw[0] and not w.any()
+    np.testing.assert_array_equal(fs[0, 0], inp[0, D:].astype(np.float64) + ape[0])
+    np.testing.assert_array_equal(fs[0, 1], 1.0)
+    np.testing.assert_array_equal(fs[0, 2], inp[0, :D])
+
+
+# -------------------------------------------------------------- segmenter
+@pytest.mark.parametrize("case", json.load(open(os.path.join(GOLDEN, "plan_examples.json")))["cases"],
+                         ids=lambda c: c["name"])
+def test_segmenter_golden(ora, case):
+    c, w = ora.plan_segments(np.array(case["seq_lens"]), np.array(case["extend_lens"]))
+    assert c.tolist() == case["compress"]
+    assert w.tolist() == case["write"]
+
+
+def test_segmenter_invariants_brute_force(ora):
+    rng = np.random.default_rng(23)
+    for _ in range(300):
+        B = int(rng.integers(1, 4))
+        ext = rng.integers(1, 301, B)
+        pre = rng.integers(0, 301, B)
+        seq = pre + ext
+        c, w = ora.plan_segments(seq, ext)
+        cover = np.zeros(int(ext.sum()), int)
+        base = np.concatenate([[0], np.cumsum(ext)])
+        for kind, rows in (("c", c.astype(np.int64)), ("w", w.astype(np.int64))):
+            for rid, b, pos, wl in rows:
+                assert 1 <= wl <= 128
+                first_pos = pos - wl + 1
+                assert first_pos // 128 == pos // 128
+                assert (pos % 128 == 127) == (kind == "c")
+                assert pre[b] <= first_pos and pos < seq[b]
+                assert rid - (pos - pre[b]) == base[b]
+                cover[rid - wl + 1: rid + 1] += 1
+        assert np.all(cover == 1)
+        assert np.all(np.bincount(w[:, 1], minlength=B) <= 1) if len(w) else True
