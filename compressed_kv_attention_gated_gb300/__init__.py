@@ -1,0 +1,16 @@
+"""Gated-softmax KV compression for NVIDIA GB300 (sm_103a).
+
+The CUDA library ``_lib/libckv.so`` (C ABI in ``include/ckv.h``) holds the
+kernels; ``ckv`` is its thin ctypes binding; ``synth`` builds seeded synthetic
+inputs of the workloads the library is measured on.
+"""
+from .ckv import (  # noqa: F401
+    CkvError,
+    ckv_c128_online_decode,
+    ckv_c128_online_prefill,
+    ckv_kpool_compress,
+    ckv_kpool_decode_update,
+    ckv_kpool_seed_tail,
+    ckv_plan_online_prefill,
+    load,
+)

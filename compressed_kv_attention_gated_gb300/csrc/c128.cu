@@ -1,0 +1,319 @@
+// c128.cu -- online P=128 gated-softmax compression (decode and prefill).
+//
+// Source: sglang page "sgl-project--sglang/.../deepseek_v4/c128_online.cuh"
+// (flash_c128_online_decode, c128_prefill_forward, flash_c128_online_prefill,
+// run_decode, run_prefill).  State layout per slot: fp32 [3][D] = max | sum | kv
+// with kv normalised; input row: [2D] = kv | score.
+//
+// Design for sm_103a (memory bound, SIMT, no tensor cores):
+//   decode  -- one warp per request, lane l owning channels 4l + 128c; the
+//              input row is issued before the slot index is known, the slot
+//              state is skipped at chunk position 0; two ex2 per channel.
+//   prefill -- one CTA of 8 warps per (segment, 128-channel slice).  Warp w
+//              owns chunk positions [16w, 16w+16), loads them 8 tokens at a
+//              time (16-byte fp32 / 8-byte bf16 vectors, streaming hints) and
+//              reduces them two-pass in registers (one ex2 per element); the 8
+//              warp partials (max, sum, weighted sum) are merged through shared
+//              memory, then merged with the stored partial state when the
+//              segment starts mid-chunk, then stored.  Compress and write
+//              passes are two launches in stream order (optionally chained
+//              by programmatic dependent launch).
+#include "ckv_device.cuh"
+#include "ckv_launch.h"
+
+namespace ckv {
+namespace {
+
+// --------------------------------------------------------------------------
+// decode
+// --------------------------------------------------------------------------
+constexpr int kDecodeWarps = 4;
+
+template <int D, typename InT>
+__global__ void __launch_bounds__(kDecodeWarps * 32)
+    c128_decode_kernel(const __grid_constant__ C128DecodeArgs a) {
+  constexpr int C = D / 128;  // 4-channel groups per lane
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kDecodeWarps + (threadIdx.x >> 5);
+  if (b >= a.B) return;
+
+  const InT* in = static_cast<const InT*>(a.input) + static_cast<int64_t>(b) * 2 * D;
+  float4 kin[C], sin_[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) {
+    kin[c] = In4<InT>::load(in, 4 * lane + 128 * c);
+    sin_[c] = In4<InT>::load(in + D, 4 * lane + 128 * c);
+  }
+  const int32_t index = a.indices[b];
+  const int32_t seq_len = a.seq_lens[b];
+  if (seq_len < 1) {
+    if (lane == 0) flag_error(a.err, CKV_DEVERR_SEQ_LEN);
+    return;
+  }
+  if (index < 0 || index >= a.num_slots) {
+    if (lane == 0) flag_error(a.err, CKV_DEVERR_SLOT);
+    return;
+  }
+  const int p = (seq_len - 1) & 127;  // chunk position of the new token
+  float* st = a.state + static_cast<int64_t>(index) * 3 * D;
+
+  float4 ap[C], om[C], os[C], okv[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) ap[c] = ld_shared_ro_f4(a.ape + p * D + 4 * lane + 128 * c);
+  if (p != 0) {
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      const int col = 4 * lane + 128 * c;
+      om[c] = *reinterpret_cast<const float4*>(st + col);
+      os[c] = *reinterpret_cast<const float4*>(st + D + col);
+      okv[c] = *reinterpret_cast<const float4*>(st + 2 * D + col);
+    }
+  }
+  float4 nm[C], ns[C], nkv[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float z = get(sin_[c], i) + get(ap[c], i);
+      const float k = get(kin[c], i);
+      if (p == 0) {
+        set(nm[c], i, z);
+        set(ns[c], i, 1.f);
+        set(nkv[c], i, k);
+      } else {
+        const float m1 = get(om[c], i);
+        const float M = fmaxf(m1, z);
+        const float w1 = get(os[c], i) * exp_diff(m1, M);
+        const float w2 = exp_diff(z, M);
+        const float s = w1 + w2;
+        set(nm[c], i, M);
+        set(ns[c], i, s);
+        set(nkv[c], i, (get(okv[c], i) * w1 + k * w2) / s);
+      }
+    }
+  }
+  if (p == 127) {
+    float* o = a.out + static_cast<int64_t>(b) * D;
+#pragma unroll
+    for (int c = 0; c < C; ++c) reinterpret_cast<float4*>(o + 128 * c)[lane] = nkv[c];
+  } else {
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      const int col = 4 * lane + 128 * c;
+      *reinterpret_cast<float4*>(st + col) = nm[c];
+      *reinterpret_cast<float4*>(st + D + col) = ns[c];
+      *reinterpret_cast<float4*>(st + 2 * D + col) = nkv[c];
+    }
+  }
+}
+
+// --------------------------------------------------------------------------
+// prefill
+// --------------------------------------------------------------------------
+constexpr int kPrefillWarps = 8;                 // warps per CTA
+constexpr int kPosPerWarp = 128 / kPrefillWarps; // chunk positions per warp
+constexpr int kBatch = 8;                        // tokens loaded per round
+
+template <int D, typename InT, bool kWrite>
+__global__ void __launch_bounds__(kPrefillWarps * 32, 2)
+    c128_prefill_kernel(const __grid_constant__ C128PrefillArgs a) {
+  constexpr int S = D / 128;  // 128-channel slices per row
+  __shared__ __align__(16) float4 s_m[kPrefillWarps][32];
+  __shared__ __align__(16) float4 s_s[kPrefillWarps][32];
+  __shared__ __align__(16) float4 s_a[kPrefillWarps][32];
+
+  pdl_wait();
+  const uint32_t plan_id = blockIdx.x / S;
+  const int slice = blockIdx.x % S;
+  const uint32_t n_plans = kWrite ? a.num_write : a.num_compress;
+  if (plan_id >= n_plans) return;
+  const uint4 raw = *reinterpret_cast<const uint4*>(kWrite ? a.write_plan + plan_id
+                                                           : a.compress_plan + plan_id);
+  pdl_trigger();
+  const uint32_t ragged_id = raw.x, batch = raw.y, position = raw.z, window = raw.w;
+  if (ragged_id == 0xFFFFFFFFu) return;  // sentinel (graph padding)
+
+  const uint32_t pic = position & 127u;  // chunk position of the last token
+  const bool plan_ok = batch < static_cast<uint32_t>(a.B) && window >= 1 && window <= pic + 1 &&
+                       ragged_id < a.num_tokens && ragged_id + 1 >= window &&
+                       (kWrite ? (pic != 127u) : (pic == 127u));
+  if (!plan_ok) {
+    if (threadIdx.x == 0) flag_error(a.err, CKV_DEVERR_PLAN);
+    return;
+  }
+  const int chunk_offset = static_cast<int>(pic + 1 - window);
+  const int window_end = static_cast<int>(pic + 1);
+  int32_t load_index = -1, store_index = -1;
+  if (chunk_offset != 0) load_index = a.load_indices[batch];
+  if (kWrite) store_index = a.indices[batch];
+  if ((chunk_offset != 0 && (load_index < 0 || load_index >= a.num_slots)) ||
+      (kWrite && (store_index < 0 || store_index >= a.num_slots))) {
+    if (threadIdx.x == 0) flag_error(a.err, CKV_DEVERR_SLOT);
+    return;
+  }
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col = slice * 128 + 4 * lane;
+  const int64_t row_c0 = static_cast<int64_t>(ragged_id) - pic;  // ragged row of chunk position 0
+  const InT* in = static_cast<const InT*>(a.input);
+
+  float M[4] = {kNegBig, kNegBig, kNegBig, kNegBig};
+  float Ssum[4] = {0.f, 0.f, 0.f, 0.f}, A[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int r = 0; r < kPosPerWarp / kBatch; ++r) {
+    const int j0 = warp * kPosPerWarp + r * kBatch;
+    if (j0 >= window_end || j0 + kBatch <= chunk_offset) continue;  // warp-uniform
+    float4 kv[kBatch], sc[kBatch], ap[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int j = j0 + i;
+      if (j >= chunk_offset && j < window_end) {
+        const InT* row = in + (row_c0 + j) * 2 * D;
+        kv[i] = In4<InT>::load(row, col);
+        sc[i] = In4<InT>::load(row + D, col);
+        ap[i] = ld_shared_ro_f4(a.ape + j * D + col);
+      } else {
+        kv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        sc[i] = make_float4(kNegBig, kNegBig, kNegBig, kNegBig);
+        ap[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float z[kBatch];
+      float bm = kNegBig;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        z[i] = get(sc[i], c) + get(ap[i], c);
+        bm = fmaxf(bm, z[i]);
+      }
+      float bs = 0.f, ba = 0.f;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int j = j0 + i;
+        const float e = (j >= chunk_offset && j < window_end) ? exp_diff(z[i], bm) : 0.f;
+        bs += e;
+        ba = fmaf(e, get(kv[i], c), ba);
+      }
+      const float nm = fmaxf(M[c], bm);
+      const float f1 = exp_diff(M[c], nm), f2 = exp_diff(bm, nm);
+      Ssum[c] = Ssum[c] * f1 + bs * f2;
+      A[c] = A[c] * f1 + ba * f2;
+      M[c] = nm;
+    }
+  }
+  s_m[warp][lane] = make_float4(M[0], M[1], M[2], M[3]);
+  s_s[warp][lane] = make_float4(Ssum[0], Ssum[1], Ssum[2], Ssum[3]);
+  s_a[warp][lane] = make_float4(A[0], A[1], A[2], A[3]);
+  __syncthreads();
+  if (threadIdx.x >= 128) return;
+
+  // Channel t of the slice: merge the 8 warp partials, then the stored partial.
+  const int t = threadIdx.x;
+  const float* fm = reinterpret_cast<const float*>(s_m);
+  const float* fs = reinterpret_cast<const float*>(s_s);
+  const float* fa = reinterpret_cast<const float*>(s_a);
+  float m = kNegBig;
+#pragma unroll
+  for (int w = 0; w < kPrefillWarps; ++w) m = fmaxf(m, fm[w * 128 + t]);
+  float ssum = 0.f, acc = 0.f;
+#pragma unroll
+  for (int w = 0; w < kPrefillWarps; ++w) {
+    const float f = exp_diff(fm[w * 128 + t], m);
+    ssum = fmaf(fs[w * 128 + t], f, ssum);
+    acc = fmaf(fa[w * 128 + t], f, acc);
+  }
+  float kv = acc / ssum;
+  const int ch = slice * 128 + t;
+  if (chunk_offset != 0) {
+    const float* ld = a.state + static_cast<int64_t>(load_index) * 3 * D + ch;
+    const float m1 = ld[0], s1 = ld[D], k1 = ld[2 * D];
+    const float nm = fmaxf(m1, m);
+    const float w1 = s1 * exp_diff(m1, nm), w2 = ssum * exp_diff(m, nm);
+    ssum = w1 + w2;
+    kv = (k1 * w1 + kv * w2) / ssum;
+    m = nm;
+  }
+  if (kWrite) {
+    float* stp = a.state + static_cast<int64_t>(store_index) * 3 * D + ch;
+    stp[0] = m;
+    stp[D] = ssum;
+    stp[2 * D] = kv;
+  } else {
+    a.out[static_cast<int64_t>(ragged_id) * D + ch] = kv;
+  }
+}
+
+template <typename Args>
+cudaError_t launch(void (*k)(Args), dim3 grid, dim3 block, bool use_pdl, cudaStream_t s,
+                   const Args& args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = use_pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, args);
+}
+
+template <int D, typename InT>
+cudaError_t decode_d(const C128DecodeArgs& a, bool use_pdl, cudaStream_t s) {
+  const dim3 grid((a.B + kDecodeWarps - 1) / kDecodeWarps);
+  return launch(c128_decode_kernel<D, InT>, grid, dim3(kDecodeWarps * 32), use_pdl, s, a);
+}
+
+template <int D, typename InT>
+cudaError_t prefill_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
+  constexpr int S = D / 128;
+  if (a.num_compress) {
+    const dim3 grid(static_cast<unsigned>(a.num_compress) * S);
+    cudaError_t e = launch(c128_prefill_kernel<D, InT, false>, grid, dim3(kPrefillWarps * 32),
+                           use_pdl, s, a);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.num_write) {
+    const dim3 grid(static_cast<unsigned>(a.num_write) * S);
+    cudaError_t e = launch(c128_prefill_kernel<D, InT, true>, grid, dim3(kPrefillWarps * 32),
+                           use_pdl, s, a);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_c128_decode(const C128DecodeArgs& a, int D, int in_dtype, bool use_pdl,
+                               cudaStream_t s) {
+  if (in_dtype == CKV_F32) {
+    if (D == 128) return decode_d<128, float>(a, use_pdl, s);
+    if (D == 256) return decode_d<256, float>(a, use_pdl, s);
+    if (D == 512) return decode_d<512, float>(a, use_pdl, s);
+  } else {
+    if (D == 128) return decode_d<128, __nv_bfloat16>(a, use_pdl, s);
+    if (D == 256) return decode_d<256, __nv_bfloat16>(a, use_pdl, s);
+    if (D == 512) return decode_d<512, __nv_bfloat16>(a, use_pdl, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_c128_prefill(const C128PrefillArgs& a, int D, int in_dtype, bool use_pdl,
+                                cudaStream_t s) {
+  if (in_dtype == CKV_F32) {
+    if (D == 128) return prefill_d<128, float>(a, use_pdl, s);
+    if (D == 256) return prefill_d<256, float>(a, use_pdl, s);
+    if (D == 512) return prefill_d<512, float>(a, use_pdl, s);
+  } else {
+    if (D == 128) return prefill_d<128, __nv_bfloat16>(a, use_pdl, s);
+    if (D == 256) return prefill_d<256, __nv_bfloat16>(a, use_pdl, s);
+    if (D == 512) return prefill_d<512, __nv_bfloat16>(a, use_pdl, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace ckv

@@ -1,0 +1,229 @@
+// capi.cu -- the extern "C" entry points declared in include/ckv.h.
+//
+// Every entry point checks its sizes, flags and pointer alignment on the host,
+// fills an argument block and enqueues the kernels on the caller's stream.
+// Nothing is allocated and nothing synchronises.
+#include <cstdint>
+
+#include "ckv.h"
+#include "ckv_launch.h"
+
+namespace {
+
+thread_local int32_t g_last_cuda_error = 0;
+
+ckv_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return CKV_OK;
+  g_last_cuda_error = static_cast<int32_t>(e);
+  return CKV_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool pool_size_ok(int32_t P) { return P == 1 || P == 2 || P == 4 || P == 8 || P == 16; }
+bool head_dim_ok(int32_t D) { return D == 128 || D == 256 || D == 512; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t ckv_abi_version(void) { return 1; }
+
+int32_t ckv_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* ckv_status_string(ckv_status s) {
+  switch (s) {
+    case CKV_OK: return "ok";
+    case CKV_ERR_NULL: return "a required pointer is NULL";
+    case CKV_ERR_SHAPE: return "unsupported or inconsistent size, stride or flag";
+    case CKV_ERR_DTYPE: return "unsupported input dtype";
+    case CKV_ERR_ALIGN: return "pointer or stride breaks the 16-byte alignment rule";
+    case CKV_ERR_PLAN: return "planner: invalid lengths, token count or capacity";
+    case CKV_ERR_CUDA: return "CUDA runtime error (see ckv_last_cuda_error)";
+    default: return "unknown status";
+  }
+}
+
+ckv_status ckv_kpool_decode_update(uint8_t* kv_cache, int64_t num_pages, int32_t page_size,
+                                   uint16_t* tail_ring, int64_t num_tail_blocks,
+                                   const int32_t* tail_slot_mapping, const int32_t* slot_mapping,
+                                   const int32_t* positions, const uint16_t* key,
+                                   int64_t key_stride_b, int64_t key_stride_t,
+                                   const uint16_t* score, int64_t score_stride_b,
+                                   int64_t score_stride_t, const float* ape, int32_t B, int32_t N,
+                                   int32_t P, int32_t D, int32_t round_scale, float* tap_x,
+                                   uint16_t* tap_xb, uint16_t* tap_yb, int32_t* err_word,
+                                   void* stream) {
+  if (B < 0 || N < 0 || D != 128 || !pool_size_ok(P) || page_size <= 0 || num_pages < 0 ||
+      num_tail_blocks < 0)
+    return CKV_ERR_SHAPE;
+  if (B == 0 || N == 0) return CKV_OK;
+  if (!kv_cache || !tail_ring || !tail_slot_mapping || !slot_mapping || !positions || !key ||
+      !score || !ape)
+    return CKV_ERR_NULL;
+  if (key_stride_b < 0 || key_stride_t < 0 || score_stride_b < 0 || score_stride_t < 0)
+    return CKV_ERR_SHAPE;
+  if (!aligned(kv_cache, 16) || !aligned(tail_ring, 16) || !aligned(key, 16) ||
+      !aligned(score, 16) || !aligned(ape, 16) || key_stride_b % 8 || key_stride_t % 8 ||
+      score_stride_b % 8 || score_stride_t % 8 || !aligned(tap_x, 16) || !aligned(tap_xb, 8) ||
+      !aligned(tap_yb, 8))
+    return CKV_ERR_ALIGN;
+  ckv::KpoolDecodeArgs a{};
+  a.cache = kv_cache;
+  a.num_pages = num_pages;
+  a.page_size = page_size;
+  a.ring = tail_ring;
+  a.num_blocks = num_tail_blocks;
+  a.tail_slot_mapping = tail_slot_mapping;
+  a.slot_mapping = slot_mapping;
+  a.positions = positions;
+  a.key = key;
+  a.key_sb = key_stride_b;
+  a.key_st = key_stride_t;
+  a.score = score;
+  a.score_sb = score_stride_b;
+  a.score_st = score_stride_t;
+  a.ape = ape;
+  a.tap_x = tap_x;
+  a.tap_xb = tap_xb;
+  a.tap_yb = tap_yb;
+  a.err = err_word;
+  a.B = B;
+  a.N = N;
+  return cuda_status(ckv::launch_kpool_decode_update(a, P, round_scale != 0,
+                                                     static_cast<cudaStream_t>(stream)));
+}
+
+ckv_status ckv_kpool_compress(uint8_t* kv_cache, int64_t num_pages, int32_t page_size,
+                              const uint16_t* slot_k, const uint16_t* slot_score, const float* ape,
+                              const int64_t* loc, const uint8_t* write_mask, int32_t write_cache,
+                              uint8_t* out_fp8, float* out_scale, int64_t n_pools, int32_t P,
+                              int32_t D, int32_t round_scale, float* tap_x, uint16_t* tap_xb,
+                              uint16_t* tap_yb, int32_t* err_word, void* stream) {
+  if (n_pools < 0 || D != 128 || !pool_size_ok(P)) return CKV_ERR_SHAPE;
+  if (!write_cache && !out_fp8) return CKV_ERR_SHAPE;        // nothing requested
+  if ((out_fp8 == nullptr) != (out_scale == nullptr)) return CKV_ERR_NULL;
+  if (write_mask && out_fp8) return CKV_ERR_SHAPE;           // masked rows have no output
+  if (write_cache && (page_size <= 0 || num_pages < 0)) return CKV_ERR_SHAPE;
+  if (n_pools == 0) return CKV_OK;
+  if (n_pools > (static_cast<int64_t>(INT32_MAX) / 32) * 8) return CKV_ERR_SHAPE;
+  if (!slot_k || !slot_score || !ape || (write_cache && (!kv_cache || !loc))) return CKV_ERR_NULL;
+  if (!aligned(slot_k, 16) || !aligned(slot_score, 16) || !aligned(ape, 16) ||
+      !aligned(kv_cache, 16) || !aligned(out_fp8, 16) || !aligned(tap_x, 16) ||
+      !aligned(tap_xb, 8) || !aligned(tap_yb, 8) || !aligned(loc, 8))
+    return CKV_ERR_ALIGN;
+  ckv::KpoolCompressArgs a{};
+  a.cache = kv_cache;
+  a.num_pages = num_pages;
+  a.page_size = page_size > 0 ? page_size : 1;
+  a.slot_k = slot_k;
+  a.slot_score = slot_score;
+  a.ape = ape;
+  a.loc = loc;
+  a.write_mask = write_mask;
+  a.out_fp8 = out_fp8;
+  a.out_scale = out_scale;
+  a.tap_x = tap_x;
+  a.tap_xb = tap_xb;
+  a.tap_yb = tap_yb;
+  a.err = err_word;
+  a.n_pools = n_pools;
+  a.write_cache = write_cache != 0;
+  return cuda_status(
+      ckv::launch_kpool_compress(a, P, round_scale != 0, static_cast<cudaStream_t>(stream)));
+}
+
+ckv_status ckv_kpool_seed_tail(uint16_t* tail_ring, int64_t num_tail_blocks, const uint16_t* key,
+                               const uint16_t* score, const int32_t* tslot, int64_t n_tokens,
+                               int32_t P, int32_t D, int32_t* err_word, void* stream) {
+  if (n_tokens < 0 || num_tail_blocks < 0 || D != 128 || !pool_size_ok(P)) return CKV_ERR_SHAPE;
+  if (n_tokens == 0) return CKV_OK;
+  if (n_tokens > (static_cast<int64_t>(INT32_MAX) / 32) * 8) return CKV_ERR_SHAPE;
+  if (!tail_ring || !key || !score || !tslot) return CKV_ERR_NULL;
+  if (!aligned(tail_ring, 16) || !aligned(key, 16) || !aligned(score, 16)) return CKV_ERR_ALIGN;
+  ckv::KpoolSeedArgs a{};
+  a.ring = tail_ring;
+  a.num_blocks = num_tail_blocks;
+  a.key = key;
+  a.score = score;
+  a.tslot = tslot;
+  a.n_tokens = n_tokens;
+  a.err = err_word;
+  return cuda_status(ckv::launch_kpool_seed_tail(a, P, static_cast<cudaStream_t>(stream)));
+}
+
+ckv_status ckv_c128_online_decode(float* state, int64_t num_slots, const void* input,
+                                  ckv_dtype in_dtype, float* out, const float* ape,
+                                  const int32_t* indices, const int32_t* seq_lens, int32_t B,
+                                  int32_t D, int32_t use_pdl, int32_t* err_word, void* stream) {
+  if (B < 0 || num_slots < 0 || !head_dim_ok(D)) return CKV_ERR_SHAPE;
+  if (in_dtype != CKV_F32 && in_dtype != CKV_BF16) return CKV_ERR_DTYPE;
+  if (B == 0) return CKV_OK;
+  if (!state || !input || !out || !ape || !indices || !seq_lens) return CKV_ERR_NULL;
+  if (!aligned(state, 16) || !aligned(input, 16) || !aligned(out, 16) || !aligned(ape, 16))
+    return CKV_ERR_ALIGN;
+  ckv::C128DecodeArgs a{};
+  a.state = state;
+  a.num_slots = num_slots;
+  a.input = input;
+  a.out = out;
+  a.ape = ape;
+  a.indices = indices;
+  a.seq_lens = seq_lens;
+  a.err = err_word;
+  a.B = B;
+  return cuda_status(ckv::launch_c128_decode(a, D, in_dtype, use_pdl != 0,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+ckv_status ckv_c128_online_prefill(float* state, int64_t num_slots, const void* input,
+                                   ckv_dtype in_dtype, int64_t num_tokens, float* out,
+                                   const float* ape, const int32_t* indices,
+                                   const int32_t* load_indices, int32_t B,
+                                   const ckv_plan_entry* compress_plan, uint32_t num_compress,
+                                   const ckv_plan_entry* write_plan, uint32_t num_write, int32_t D,
+                                   int32_t use_pdl, int32_t* err_word, void* stream) {
+  if (B < 0 || num_slots < 0 || num_tokens < 0 || num_tokens > static_cast<int64_t>(UINT32_MAX) ||
+      !head_dim_ok(D))
+    return CKV_ERR_SHAPE;
+  if (in_dtype != CKV_F32 && in_dtype != CKV_BF16) return CKV_ERR_DTYPE;
+  if (num_compress == 0 && num_write == 0) return CKV_OK;
+  const uint64_t S = static_cast<uint64_t>(D / 128);
+  if (static_cast<uint64_t>(num_compress) * S > static_cast<uint64_t>(INT32_MAX) ||
+      static_cast<uint64_t>(num_write) * S > static_cast<uint64_t>(INT32_MAX))
+    return CKV_ERR_SHAPE;
+  if (!state || !input || !ape || !indices) return CKV_ERR_NULL;
+  if ((num_compress && (!compress_plan || !out)) || (num_write && !write_plan)) return CKV_ERR_NULL;
+  if (!aligned(state, 16) || !aligned(input, 16) || !aligned(out, 16) || !aligned(ape, 16) ||
+      !aligned(compress_plan, 16) || !aligned(write_plan, 16))
+    return CKV_ERR_ALIGN;
+  ckv::C128PrefillArgs a{};
+  a.state = state;
+  a.num_slots = num_slots;
+  a.input = input;
+  a.num_tokens = num_tokens;
+  a.out = out;
+  a.ape = ape;
+  a.indices = indices;
+  a.load_indices = load_indices ? load_indices : indices;
+  a.compress_plan = compress_plan;
+  a.write_plan = write_plan;
+  a.err = err_word;
+  a.num_compress = num_compress;
+  a.num_write = num_write;
+  a.B = B;
+  return cuda_status(ckv::launch_c128_prefill(a, D, in_dtype, use_pdl != 0,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+ckv_status ckv_plan_online_prefill(const int64_t* seq_lens, const int64_t* extend_lens, uint32_t B,
+                                   uint32_t num_tokens, ckv_plan_entry* compress_plan,
+                                   ckv_plan_entry* write_plan, int32_t pad_for_graph,
+                                   uint32_t* num_compress, uint32_t* num_write) {
+  if (!num_compress || !num_write) return CKV_ERR_NULL;
+  if (B > 0 && (!seq_lens || !extend_lens)) return CKV_ERR_NULL;
+  if (num_tokens > 0 && (!compress_plan || !write_plan)) return CKV_ERR_NULL;
+  return ckv::plan_online_prefill_host(seq_lens, extend_lens, B, num_tokens, compress_plan,
+                                       write_plan, pad_for_graph != 0, num_compress, num_write);
+}
+
+}  // extern "C"

@@ -1,0 +1,110 @@
+// ckv_launch.h -- argument blocks and launchers behind the C ABI (internal).
+//
+// Each argument block is passed to its kernel by value as a __grid_constant__
+// parameter; the C-ABI layer in capi.cu validates sizes before filling it.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ckv.h"
+
+namespace ckv {
+
+struct KpoolCompressArgs {
+  uint8_t* cache;
+  int64_t num_pages;
+  int64_t page_size;
+  const uint16_t* slot_k;
+  const uint16_t* slot_score;
+  const float* ape;
+  const int64_t* loc;
+  const uint8_t* write_mask;
+  uint8_t* out_fp8;
+  float* out_scale;
+  float* tap_x;
+  uint16_t* tap_xb;
+  uint16_t* tap_yb;
+  int32_t* err;
+  int64_t n_pools;
+  int32_t write_cache;
+};
+
+struct KpoolDecodeArgs {
+  uint8_t* cache;
+  int64_t num_pages;
+  int64_t page_size;
+  uint16_t* ring;
+  int64_t num_blocks;
+  const int32_t* tail_slot_mapping;
+  const int32_t* slot_mapping;
+  const int32_t* positions;
+  const uint16_t* key;
+  int64_t key_sb, key_st;
+  const uint16_t* score;
+  int64_t score_sb, score_st;
+  const float* ape;
+  float* tap_x;
+  uint16_t* tap_xb;
+  uint16_t* tap_yb;
+  int32_t* err;
+  int32_t B, N;
+};
+
+struct KpoolSeedArgs {
+  uint16_t* ring;
+  int64_t num_blocks;
+  const uint16_t* key;
+  const uint16_t* score;
+  const int32_t* tslot;
+  int64_t n_tokens;
+  int32_t* err;
+};
+
+struct C128DecodeArgs {
+  float* state;
+  int64_t num_slots;
+  const void* input;
+  float* out;
+  const float* ape;
+  const int32_t* indices;
+  const int32_t* seq_lens;
+  int32_t* err;
+  int32_t B;
+};
+
+struct C128PrefillArgs {
+  float* state;
+  int64_t num_slots;
+  const void* input;
+  int64_t num_tokens;
+  float* out;
+  const float* ape;
+  const int32_t* indices;
+  const int32_t* load_indices;
+  const ckv_plan_entry* compress_plan;
+  const ckv_plan_entry* write_plan;
+  int32_t* err;
+  uint32_t num_compress;
+  uint32_t num_write;
+  int32_t B;
+};
+
+cudaError_t launch_kpool_compress(const KpoolCompressArgs& a, int P, bool round_scale,
+                                  cudaStream_t s);
+cudaError_t launch_kpool_decode_update(const KpoolDecodeArgs& a, int P, bool round_scale,
+                                       cudaStream_t s);
+cudaError_t launch_kpool_seed_tail(const KpoolSeedArgs& a, int P, cudaStream_t s);
+cudaError_t launch_c128_decode(const C128DecodeArgs& a, int D, int in_dtype, bool use_pdl,
+                               cudaStream_t s);
+cudaError_t launch_c128_prefill(const C128PrefillArgs& a, int D, int in_dtype, bool use_pdl,
+                                cudaStream_t s);
+
+// Host planner (planner.cpp).
+ckv_status plan_online_prefill_host(const int64_t* seq_lens, const int64_t* extend_lens,
+                                    uint32_t B, uint32_t num_tokens,
+                                    ckv_plan_entry* compress_plan, ckv_plan_entry* write_plan,
+                                    bool pad_for_graph, uint32_t* num_compress,
+                                    uint32_t* num_write);
+
+}  // namespace ckv

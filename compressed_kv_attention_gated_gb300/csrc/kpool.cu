@@ -1,0 +1,339 @@
+// kpool.cu -- pooled (P <= 16, D = 128) gated-softmax compression kernels.
+//
+// Source: vLLM page "vllm.models.glm5next.amd.ops.kpool_compress"
+// (_kpool_decode_update_batched_kernel, _kpool_softmax_rotate_write_cache_kernel,
+// _kpool_tail_seed_kernel).  Those are AMD Triton kernels with one program per
+// request/pool and a 128-wide block; the design here is our own for sm_103a:
+//
+//   * one warp per pool (or per request), lane l owning channels 4l..4l+3, so
+//     every key/score slot row (256 B of bf16) is one coalesced 8-byte-per-lane
+//     load and every FP8 output row (128 B) one 4-byte-per-lane store;
+//   * all P slot rows of a pool are loaded before any arithmetic (P * 16 B in
+//     flight per lane), the per-slot bias table is staged in shared memory once
+//     per CTA;
+//   * exact two-pass softmax from registers: z = score + ape for the P slots,
+//     max, then one ex2 per element;
+//   * Hadamard-128: two butterfly spans inside the lane (1, 2), then five
+//     warp-shuffle spans (4..64 = lane masks 1..16), ascending; warp-shuffle
+//     absmax; fused FP8-e4m3 packing (cvt.rn.satfinite) and cache write.
+//
+// The pooled path is memory bound (no dense contraction); no tensor cores.
+#include "ckv_device.cuh"
+#include "ckv_launch.h"
+
+namespace ckv {
+namespace {
+
+constexpr int kD = 128;          // pooled head dim (the rotation is 128-point)
+constexpr int kRowBytes = kD + 4; // FP8 row + fp32 scale per cache row
+
+// Softmax-weighted pool of P slots for the lane's 4 channels.
+// kr/sr: slot rows of keys/scores, 4 bf16 each; s_ape: [P][128] fp32 in smem.
+template <int P>
+__device__ __forceinline__ void pool_softmax(const uint2 (&kr)[P], const uint2 (&sr)[P],
+                                             const float* s_ape, int lane, float (&x)[4]) {
+  float z[P][4];
+  float m[4] = {kNegBig, kNegBig, kNegBig, kNegBig};
+#pragma unroll
+  for (int j = 0; j < P; ++j) {
+    const float4 a = reinterpret_cast<const float4*>(s_ape + j * kD)[lane];
+    z[j][0] = bf16_lo(sr[j].x) + a.x;
+    z[j][1] = bf16_hi(sr[j].x) + a.y;
+    z[j][2] = bf16_lo(sr[j].y) + a.z;
+    z[j][3] = bf16_hi(sr[j].y) + a.w;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], z[j][i]);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float den = 0.f, acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+      const uint32_t w = (i < 2) ? kr[j].x : kr[j].y;
+      const float k = (i & 1) ? bf16_hi(w) : bf16_lo(w);
+      const float e = exp_diff(z[j][i], m[i]);
+      den += e;
+      acc = fmaf(e, k, acc);
+    }
+    x[i] = acc / den;
+  }
+}
+
+// x (fp32) -> bf16 -> Hadamard-128 (fp32) -> bf16 -> absmax FP8-e4m3 + scale.
+// The rotation is the orthonormal Sylvester Hadamard matrix: butterfly spans
+// 1, 2, 4, ..., 64 in ascending order, each (u + v, u - v) in fp32, then one
+// multiply by fp32(1/sqrt(128)).
+template <bool kRound>
+__device__ __forceinline__ void rotate_quantize(const float (&x)[4], int lane, uint32_t& codes,
+                                                float& scale, float (&xb)[4], float (&yb)[4]) {
+  float a[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    xb[i] = round_bf16(x[i]);
+    a[i] = xb[i];
+  }
+  {  // span 1: channel pairs (0,1), (2,3) of the lane
+    const float u0 = a[0], v0 = a[1], u1 = a[2], v1 = a[3];
+    a[0] = u0 + v0;
+    a[1] = u0 - v0;
+    a[2] = u1 + v1;
+    a[3] = u1 - v1;
+  }
+  {  // span 2: pairs (0,2), (1,3)
+    const float u0 = a[0], v0 = a[2], u1 = a[1], v1 = a[3];
+    a[0] = u0 + v0;
+    a[2] = u0 - v0;
+    a[1] = u1 + v1;
+    a[3] = u1 - v1;
+  }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {  // spans 4, 8, 16, 32, 64: partner lane l ^ m
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float o = __shfl_xor_sync(0xFFFFFFFFu, a[i], m);
+      a[i] = upper ? (o - a[i]) : (a[i] + o);
+    }
+  }
+  const float c = __uint_as_float(0x3DB504F3u);  // fp32(1/sqrt(128))
+  float am = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    yb[i] = round_bf16(a[i] * c);
+    am = fmaxf(am, fabsf(yb[i]));
+  }
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, m));
+  am = fmaxf(am, 1e-4f);
+  const float v = am * __uint_as_float(0x3B124925u);  // absmax * fp32(1/448)
+  if (kRound) {
+    // smallest power of two >= v (v is a positive normal number)
+    const uint32_t bits = __float_as_uint(v);
+    scale = (bits & 0x007FFFFFu) ? __uint_as_float((bits & 0x7F800000u) + 0x00800000u) : v;
+  } else {
+    scale = v;
+  }
+  float q[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q[i] = fminf(fmaxf(__fdiv_rn(yb[i], scale), -448.f), 448.f);
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(q[0], q[1]), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(q[2], q[3]), __NV_SATFINITE, __NV_E4M3);
+  codes = (lo & 0xFFFFu) | (hi << 16);
+}
+
+__device__ __forceinline__ void write_taps(float* tx, uint16_t* txb, uint16_t* tyb, int64_t row,
+                                           int lane, const float (&x)[4], const float (&xb)[4],
+                                           const float (&yb)[4]) {
+  if (tx) reinterpret_cast<float4*>(tx + row * kD)[lane] = make_float4(x[0], x[1], x[2], x[3]);
+  if (txb)
+    reinterpret_cast<uint2*>(txb + row * kD)[lane] =
+        make_uint2(pack_bf16x2_rn(xb[0], xb[1]), pack_bf16x2_rn(xb[2], xb[3]));
+  if (tyb)
+    reinterpret_cast<uint2*>(tyb + row * kD)[lane] =
+        make_uint2(pack_bf16x2_rn(yb[0], yb[1]), pack_bf16x2_rn(yb[2], yb[3]));
+}
+
+__device__ __forceinline__ void cache_write(uint8_t* cache, int64_t page_size, int64_t loc,
+                                            int lane, uint32_t codes, float scale) {
+  const int64_t page = loc / page_size, tok = loc - page * page_size;
+  uint8_t* base = cache + page * page_size * kRowBytes;
+  reinterpret_cast<uint32_t*>(base + tok * kD)[lane] = codes;
+  if (lane == 0) *reinterpret_cast<float*>(base + page_size * kD + 4 * tok) = scale;
+}
+
+template <int P>
+__device__ __forceinline__ void stage_ape(float* s_ape, const float* ape) {
+  for (int i = threadIdx.x; i < P * kD / 4; i += blockDim.x)
+    reinterpret_cast<float4*>(s_ape)[i] = ld_shared_ro_f4(ape + 4 * i);
+  __syncthreads();
+}
+
+constexpr int kWarpsPerCta = 8;
+
+// One-shot pooled compression: warp w of CTA c handles pool c*8 + w.
+template <int P, bool kRound>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+    kpool_compress_kernel(const __grid_constant__ KpoolCompressArgs a) {
+  __shared__ __align__(16) float s_ape[P * kD];
+  stage_ape<P>(s_ape, a.ape);
+  const int lane = threadIdx.x & 31;
+  const int64_t pool = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  if (pool >= a.n_pools) return;
+  if (a.write_mask && a.write_mask[pool] == 0) return;
+
+  uint2 kr[P], sr[P];
+  const uint16_t* kb = a.slot_k + pool * P * kD + 4 * lane;
+  const uint16_t* sb = a.slot_score + pool * P * kD + 4 * lane;
+#pragma unroll
+  for (int j = 0; j < P; ++j) {
+    kr[j] = ld_stream_u2(kb + j * kD);
+    sr[j] = ld_stream_u2(sb + j * kD);
+  }
+  float x[4], xb[4], yb[4], scale;
+  uint32_t codes;
+  pool_softmax<P>(kr, sr, s_ape, lane, x);
+  rotate_quantize<kRound>(x, lane, codes, scale, xb, yb);
+
+  if (a.write_cache) {
+    const int64_t loc = a.loc[pool];
+    if (loc < 0 || loc >= a.num_pages * a.page_size) {
+      if (lane == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
+    } else {
+      cache_write(a.cache, a.page_size, loc, lane, codes, scale);
+    }
+  }
+  if (a.out_fp8) {
+    reinterpret_cast<uint32_t*>(a.out_fp8 + pool * kD)[lane] = codes;
+    if (lane == 0) a.out_scale[pool] = scale;
+  }
+  write_taps(a.tap_x, a.tap_xb, a.tap_yb, pool, lane, x, xb, yb);
+}
+
+// Decode / verify update: warp w of CTA c handles request c*8 + w and walks its
+// N tokens in order.  A closing token reads ring slots 0..P-2 with ordinary
+// (coherent) loads: the same lane stashed any of them earlier in this call,
+// so program order makes those stores visible.
+template <int P, bool kRound>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+    kpool_decode_kernel(const __grid_constant__ KpoolDecodeArgs a) {
+  __shared__ __align__(16) float s_ape[P * kD];
+  stage_ape<P>(s_ape, a.ape);
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (b >= a.B) return;
+  const int64_t cache_rows = a.num_pages * a.page_size;
+
+  for (int t = 0; t < a.N; ++t) {
+    const int64_t idx = static_cast<int64_t>(b) * a.N + t;
+    const int32_t loc = a.slot_mapping[idx];
+    const int32_t pos = a.positions[idx];
+    const int32_t tslot = a.tail_slot_mapping[idx];
+    const uint2 kc = ld_stream_u2(a.key + b * a.key_sb + t * a.key_st + 4 * lane);
+    const uint2 sc = ld_stream_u2(a.score + b * a.score_sb + t * a.score_st + 4 * lane);
+
+    const int slot = max(pos, 0) & (P - 1);
+    const bool pos_valid = loc >= 0 && pos >= 0;
+    const bool stash_valid = pos >= 0 && tslot >= 0;
+    const bool closes = pos_valid && slot == P - 1;
+    if (!closes && !stash_valid) continue;
+    const int64_t block = static_cast<int64_t>(max(tslot, 0)) / P;
+    if (block >= a.num_blocks) {
+      if (lane == 0) flag_error(a.err, CKV_DEVERR_TAIL_BLOCK);
+      continue;
+    }
+    uint16_t* kring = a.ring + block * 2 * P * kD;
+    uint16_t* sring = kring + P * kD;
+
+    if (closes) {
+      if (loc >= cache_rows) {
+        if (lane == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
+      } else {
+        uint2 kr[P], sr[P];
+#pragma unroll
+        for (int j = 0; j < P - 1; ++j) {
+          kr[j] = *reinterpret_cast<const uint2*>(kring + j * kD + 4 * lane);
+          sr[j] = *reinterpret_cast<const uint2*>(sring + j * kD + 4 * lane);
+        }
+        kr[P - 1] = kc;
+        sr[P - 1] = sc;
+        float x[4], xb[4], yb[4], scale;
+        uint32_t codes;
+        pool_softmax<P>(kr, sr, s_ape, lane, x);
+        rotate_quantize<kRound>(x, lane, codes, scale, xb, yb);
+        cache_write(a.cache, a.page_size, loc, lane, codes, scale);
+        write_taps(a.tap_x, a.tap_xb, a.tap_yb, idx, lane, x, xb, yb);
+      }
+    }
+    if (stash_valid) {
+      *reinterpret_cast<uint2*>(kring + slot * kD + 4 * lane) = kc;
+      *reinterpret_cast<uint2*>(sring + slot * kD + 4 * lane) = sc;
+    }
+  }
+}
+
+// Tail-ring seed: warp w of CTA c handles prefill token c*8 + w.
+template <int P>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+    kpool_seed_kernel(const __grid_constant__ KpoolSeedArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  if (i >= a.n_tokens) return;
+  const int64_t t = a.tslot[i];
+  if (t < 0) return;
+  const int64_t blk = t / P;
+  const int64_t ahead = (i + P < a.n_tokens) ? a.tslot[i + P] : -1;
+  if (ahead >= 0 && ahead / P == blk) return;  // not among the request's last P tokens
+  if (blk >= a.num_blocks) {
+    if (lane == 0) flag_error(a.err, CKV_DEVERR_TAIL_BLOCK);
+    return;
+  }
+  uint16_t* base = a.ring + blk * 2 * P * kD + (t % P) * kD;
+  reinterpret_cast<uint2*>(base)[lane] = ld_stream_u2(a.key + i * kD + 4 * lane);
+  reinterpret_cast<uint2*>(base + P * kD)[lane] = ld_stream_u2(a.score + i * kD + 4 * lane);
+}
+
+template <int P>
+cudaError_t compress_p(const KpoolCompressArgs& a, bool round_scale, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>((a.n_pools + kWarpsPerCta - 1) / kWarpsPerCta));
+  if (round_scale)
+    kpool_compress_kernel<P, true><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
+  else
+    kpool_compress_kernel<P, false><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int P>
+cudaError_t decode_p(const KpoolDecodeArgs& a, bool round_scale, cudaStream_t s) {
+  const dim3 grid((a.B + kWarpsPerCta - 1) / kWarpsPerCta);
+  if (round_scale)
+    kpool_decode_kernel<P, true><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
+  else
+    kpool_decode_kernel<P, false><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int P>
+cudaError_t seed_p(const KpoolSeedArgs& a, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>((a.n_tokens + kWarpsPerCta - 1) / kWarpsPerCta));
+  kpool_seed_kernel<P><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_kpool_compress(const KpoolCompressArgs& a, int P, bool round_scale,
+                                  cudaStream_t s) {
+  switch (P) {
+    case 1: return compress_p<1>(a, round_scale, s);
+    case 2: return compress_p<2>(a, round_scale, s);
+    case 4: return compress_p<4>(a, round_scale, s);
+    case 8: return compress_p<8>(a, round_scale, s);
+    case 16: return compress_p<16>(a, round_scale, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_kpool_decode_update(const KpoolDecodeArgs& a, int P, bool round_scale,
+                                       cudaStream_t s) {
+  switch (P) {
+    case 1: return decode_p<1>(a, round_scale, s);
+    case 2: return decode_p<2>(a, round_scale, s);
+    case 4: return decode_p<4>(a, round_scale, s);
+    case 8: return decode_p<8>(a, round_scale, s);
+    case 16: return decode_p<16>(a, round_scale, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_kpool_seed_tail(const KpoolSeedArgs& a, int P, cudaStream_t s) {
+  switch (P) {
+    case 1: return seed_p<1>(a, s);
+    case 2: return seed_p<2>(a, s);
+    case 4: return seed_p<4>(a, s);
+    case 8: return seed_p<8>(a, s);
+    case 16: return seed_p<16>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace ckv

@@ -1,0 +1,255 @@
+/*
+ * ckv.h -- C ABI of the gated-softmax KV compression library (GB300, sm_103a).
+ *
+ * The method: tokens are grouped into chunks of P consecutive positions and
+ * every channel d of a chunk's compressed key is
+ *
+ *     out[d] = sum_j softmax_j(score_j[d] + ape[j mod P][d]) * k_j[d]
+ *
+ * (a per-channel softmax over the chunk's tokens).  Two families of calls:
+ *   - pooled, P = 16 (or 1, 2, 4, 8), D = 128, bf16 keys/scores: the pooled row
+ *     is rounded to bf16, rotated by a 128-point Hadamard transform, rounded
+ *     to bf16 again and stored as FP8-e4m3 with one fp32 absmax scale in a
+ *     paged cache.  Source: vLLM page "vllm.models.glm5next.amd.ops.kpool_compress".
+ *   - online, P = 128, D in {128, 256, 512}, fp32 or bf16 inputs: a per-slot
+ *     fp32 running state (max, sum, kv) is updated one token at a time
+ *     (decode) or one segment at a time (prefill).  Source: sglang page
+ *     "sgl-project--sglang/.../jit_kernel/csrc/deepseek_v4/c128_online.cuh".
+ *
+ * Conventions for every call below:
+ *   - Pointers marked "device" are CUDA device memory owned by the caller;
+ *     "host" pointers are ordinary (or pinned) host memory.  The library
+ *     allocates nothing and never synchronises the stream.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *     only enqueued; results are visible after the stream reaches it.
+ *   - Sizes are checked on the host before anything is launched; a failed
+ *     check returns a nonzero ckv_status and launches nothing.  An empty
+ *     batch returns CKV_OK and launches nothing.
+ *   - `err_word` (device, nullable) receives, by atomic OR, a CKV_DEVERR_*
+ *     bit when a kernel meets an index that is out of range (a slot, a tail
+ *     block, a cache location, a malformed plan entry).  The offending
+ *     access is skipped, never performed; everything else proceeds.  The
+ *     word is never cleared by the library.
+ *   - Caller contract inherited from the sources: within one call, distinct
+ *     requests use distinct tail blocks, state slots and cache locations
+ *     (concurrent CTAs touch disjoint memory).  Overlapping calls on
+ *     different streams that share buffers race.
+ */
+#ifndef CKV_H_
+#define CKV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t ckv_status;
+#define CKV_OK 0
+#define CKV_ERR_NULL 1       /* a required pointer is NULL */
+#define CKV_ERR_SHAPE 2      /* unsupported or inconsistent size, stride or flag */
+#define CKV_ERR_DTYPE 3      /* unsupported input dtype */
+#define CKV_ERR_ALIGN 4      /* a pointer or stride breaks the 16-byte alignment rule */
+#define CKV_ERR_PLAN 5       /* planner: bad lengths, token count or capacity */
+#define CKV_ERR_CUDA 6       /* a CUDA runtime call failed (see ckv_last_cuda_error) */
+
+/* Bits OR-ed into err_word by the kernels (the access is skipped). */
+#define CKV_DEVERR_SLOT 0x1u       /* state slot index outside [0, num_slots) */
+#define CKV_DEVERR_TAIL_BLOCK 0x2u /* tail block outside [0, num_tail_blocks) */
+#define CKV_DEVERR_CACHE_LOC 0x4u  /* cache location outside [0, num_pages * page_size) */
+#define CKV_DEVERR_PLAN 0x8u       /* plan entry fields inconsistent or out of range */
+#define CKV_DEVERR_SEQ_LEN 0x10u   /* decode seq_len < 1 */
+
+typedef int32_t ckv_dtype;
+#define CKV_F32 0
+#define CKV_BF16 1
+
+/* One prefill segment: a run of tokens of one request inside one 128-chunk,
+ * described by its LAST token (sglang page, struct OnlinePrefillPlan):
+ *   ragged_id  row of the last token in the ragged [num_tokens, 2D] input
+ *   batch_id   request index (into indices / load_indices)
+ *   position   global position of the last token; position % 128 == 127 for
+ *              a compress (chunk-closing) segment, < 127 for a write segment
+ *   window_len number of tokens, 1..128; the first token is at ragged row
+ *              ragged_id - window_len + 1 and position position - window_len + 1
+ * An entry with all four fields 0xFFFFFFFF is a sentinel and is skipped. */
+typedef struct ckv_plan_entry {
+  uint32_t ragged_id;
+  uint32_t batch_id;
+  uint32_t position;
+  uint32_t window_len;
+} ckv_plan_entry;
+
+/* Returns a static, human-readable description of a status code. */
+const char* ckv_status_string(ckv_status s);
+
+/* The cudaError_t of the most recent CKV_ERR_CUDA on the calling thread. */
+int32_t ckv_last_cuda_error(void);
+
+/* ABI version of this header (incremented on incompatible changes). */
+int32_t ckv_abi_version(void);
+
+/*
+ * Pooled decode / speculative-verify update (vLLM kpool_compress page,
+ * _kpool_decode_update_batched_kernel and
+ * kpool_decode_update_and_maybe_write_cache_batched).
+ *
+ * For each request b (processed independently) and each of its N tokens t in
+ * order, with idx = b*N + t:
+ *   pos_valid   = slot_mapping[idx] >= 0 && positions[idx] >= 0
+ *   stash_valid = positions[idx] >= 0 && tail_slot_mapping[idx] >= 0
+ *   slot        = max(positions[idx], 0) % P;  block = max(tail_slot_mapping[idx], 0) / P
+ *   If pos_valid and slot == P-1 the pool closes: the P tokens are ring slots
+ *   0..P-2 of `block` plus the current token, and the compressed FP8 row and
+ *   scale are written to the cache at location slot_mapping[idx].  Then, if
+ *   stash_valid, the token's key and score are stored in ring slot `slot`
+ *   (after the completion read, so a pool sees tokens stashed earlier in the
+ *   same call).
+ *
+ * kv_cache          device uint8 [num_pages][page_size][D+4]: per page,
+ *                   page_size rows of D FP8-e4m3 bytes (row-major), then
+ *                   page_size fp32 scales.  Location loc is page loc/page_size,
+ *                   row loc%page_size.
+ * tail_ring         device bf16 [num_tail_blocks][2][P][D]: half 0 keys,
+ *                   half 1 gate scores; updated in place.
+ * tail_slot_mapping, slot_mapping, positions
+ *                   device int32 [B][N]; -1 marks padding.  slot_mapping is
+ *                   pool-granular (>= 0 only on a pool's last token).
+ * key, score        device bf16, row (b, t) at b*stride_b + t*stride_t
+ *                   elements, D contiguous; 16-byte aligned rows.
+ * ape               device fp32 [P][D] contiguous (per-slot position bias).
+ * P                 1, 2, 4, 8 or 16.  D must be 128.
+ * round_scale       nonzero: scale = 2^ceil(log2(absmax/448)); zero: absmax/448.
+ * tap_x, tap_xb, tap_yb
+ *                   device, nullable, [B*N][D]: the fp32 pooled row, its bf16
+ *                   rounding and the bf16 rotated row of every closing token
+ *                   (row idx); rows of other tokens are not written.
+ */
+ckv_status ckv_kpool_decode_update(uint8_t* kv_cache, int64_t num_pages, int32_t page_size,
+                                   uint16_t* tail_ring, int64_t num_tail_blocks,
+                                   const int32_t* tail_slot_mapping, const int32_t* slot_mapping,
+                                   const int32_t* positions, const uint16_t* key,
+                                   int64_t key_stride_b, int64_t key_stride_t,
+                                   const uint16_t* score, int64_t score_stride_b,
+                                   int64_t score_stride_t, const float* ape, int32_t B, int32_t N,
+                                   int32_t P, int32_t D, int32_t round_scale, float* tap_x,
+                                   uint16_t* tap_xb, uint16_t* tap_yb, int32_t* err_word,
+                                   void* stream);
+
+/*
+ * One-shot pooled compression (vLLM kpool_compress page,
+ * _kpool_softmax_rotate_write_cache_kernel and kpool_compress_and_write_cache).
+ *
+ * slot_k, slot_score device bf16 [n_pools][P][D] contiguous.
+ * ape                device fp32 [P][D].
+ * loc                device int64 [n_pools]: cache location of each pool
+ *                    (used only when write_cache != 0).
+ * write_mask         device uint8 [n_pools], nullable: pools with 0 write
+ *                    nothing (only allowed with out_fp8 == NULL).
+ * write_cache        nonzero: store rows + scales into kv_cache (layout as above).
+ * out_fp8, out_scale device, nullable together: [n_pools][D] FP8 codes and
+ *                    [n_pools] fp32 scales of every pool ("return compressed").
+ * At least one of write_cache / out_fp8 must be requested.
+ * tap_x, tap_xb, tap_yb: device, nullable, [n_pools][D] stage taps.
+ */
+ckv_status ckv_kpool_compress(uint8_t* kv_cache, int64_t num_pages, int32_t page_size,
+                              const uint16_t* slot_k, const uint16_t* slot_score, const float* ape,
+                              const int64_t* loc, const uint8_t* write_mask, int32_t write_cache,
+                              uint8_t* out_fp8, float* out_scale, int64_t n_pools, int32_t P,
+                              int32_t D, int32_t round_scale, float* tap_x, uint16_t* tap_xb,
+                              uint16_t* tap_yb, int32_t* err_word, void* stream);
+
+/*
+ * Seed the pooled tail ring from a prefill batch (vLLM kpool_compress page,
+ * _kpool_tail_seed_kernel and kpool_seed_tail_cache).  Token i with tail slot
+ * t = tslot[i] >= 0 is copied to ring[t / P][{key, score}][t % P] iff the
+ * token P places ahead (i + P) is past the batch, has a negative tail slot,
+ * or lies in another tail block -- i.e. the token is among its request's
+ * last P tokens.
+ * key, score  device bf16 [n_tokens][D] contiguous; tslot device int32 [n_tokens].
+ * tail_ring   device bf16 [num_tail_blocks][2][P][D].  P in {1,2,4,8,16}; D == 128.
+ */
+ckv_status ckv_kpool_seed_tail(uint16_t* tail_ring, int64_t num_tail_blocks, const uint16_t* key,
+                               const uint16_t* score, const int32_t* tslot, int64_t n_tokens,
+                               int32_t P, int32_t D, int32_t* err_word, void* stream);
+
+/*
+ * Online c128 decode (sglang c128_online.cuh page, flash_c128_online_decode
+ * and run_decode).  For request b: the token sits at chunk position
+ * p = (seq_lens[b] - 1) % 128 with logit z = score + ape[p].
+ *   p == 0:   state := (z, 1, kv_in)
+ *   p  > 0:   merge into the state of slot indices[b]:
+ *             M = max(m, z), s' = s*e^(m-M) + e^(z-M),
+ *             kv' = (kv*s*e^(m-M) + kv_in*e^(z-M)) / s'
+ *   p == 127: out[b] := kv' and the slot is left unchanged; otherwise the
+ *             new (max, sum, kv) is stored in slot indices[b].
+ * state       device fp32 [num_slots][3][D] laid out max | sum | kv.
+ * input       device [B][2D] laid out kv | score; fp32 (CKV_F32) or bf16 (CKV_BF16).
+ * out         device fp32 [B][D]; only rows of chunk-closing requests are written.
+ * ape         device fp32 [128][D].   indices, seq_lens: device int32 [B].
+ * D           128, 256 or 512.   Pointers 16-byte aligned.
+ * use_pdl     nonzero: launch as a programmatic dependent launch (the kernel
+ *             waits for the preceding grid before touching memory).
+ */
+ckv_status ckv_c128_online_decode(float* state, int64_t num_slots, const void* input,
+                                  ckv_dtype in_dtype, float* out, const float* ape,
+                                  const int32_t* indices, const int32_t* seq_lens, int32_t B,
+                                  int32_t D, int32_t use_pdl, int32_t* err_word, void* stream);
+
+/*
+ * Online c128 prefill (sglang c128_online.cuh page, flash_c128_online_prefill,
+ * c128_prefill_forward and run_prefill).  Two stream-ordered launches:
+ *   1. compress pass over compress_plan[0..num_compress): per segment and
+ *      channel, softmax over the segment's tokens (bias ape[chunk position]),
+ *      merged with the partial state of slot load_indices[batch_id] when the
+ *      segment does not start at chunk position 0; the result is written to
+ *      out[ragged_id].  The state buffer is only read.
+ *   2. write pass over write_plan[0..num_write): the same reduction, whose
+ *      (max, sum, kv) is stored into slot indices[batch_id].
+ * The second launch starts after every read of the first has completed, so
+ * a slot read in pass 1 may be overwritten in pass 2.
+ * state          device fp32 [num_slots][3][D].
+ * input          device [num_tokens][2D] (kv | score), fp32 or bf16.
+ * out            device fp32 [num_tokens][D]; only compress rows are written.
+ * ape            device fp32 [128][D].
+ * indices        device int32 [B]; load_indices device int32 [B] or NULL (= indices).
+ * compress_plan, write_plan
+ *                device arrays of ckv_plan_entry (16-byte aligned), e.g. from
+ *                ckv_plan_online_prefill; sentinel entries are skipped.
+ * D              128, 256 or 512.   use_pdl as for decode.
+ */
+ckv_status ckv_c128_online_prefill(float* state, int64_t num_slots, const void* input,
+                                   ckv_dtype in_dtype, int64_t num_tokens, float* out,
+                                   const float* ape, const int32_t* indices,
+                                   const int32_t* load_indices, int32_t B,
+                                   const ckv_plan_entry* compress_plan, uint32_t num_compress,
+                                   const ckv_plan_entry* write_plan, uint32_t num_write, int32_t D,
+                                   int32_t use_pdl, int32_t* err_word, void* stream);
+
+/*
+ * Host planner for the online c128 prefill (sglang c128_online.cuh page,
+ * plan_online_prefill_host).  Request i covers global positions
+ * [seq_lens[i] - extend_lens[i], seq_lens[i]) and ragged rows that follow the
+ * rows of requests 0..i-1.  The range is split at multiples of 128; a
+ * segment ending at chunk position 127 is appended to compress_plan, the
+ * trailing partial segment (at most one per request) to write_plan.
+ * seq_lens, extend_lens  host int64 [B]; 0 < extend_lens[i] <= seq_lens[i] < 2^32.
+ * num_tokens             must equal sum(extend_lens); it is also the capacity
+ *                        (rows) of each plan array.
+ * compress_plan, write_plan host (or pinned) arrays of num_tokens entries.
+ * pad_for_graph          nonzero: fill both arrays to num_tokens rows with
+ *                        sentinels and report num_tokens for both counts, so
+ *                        a captured CUDA graph always sees the same grid.
+ * num_compress, num_write host outputs.
+ * Returns CKV_ERR_PLAN (and writes no counts) on invalid lengths.
+ */
+ckv_status ckv_plan_online_prefill(const int64_t* seq_lens, const int64_t* extend_lens, uint32_t B,
+                                   uint32_t num_tokens, ckv_plan_entry* compress_plan,
+                                   ckv_plan_entry* write_plan, int32_t pad_for_graph,
+                                   uint32_t* num_compress, uint32_t* num_write);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CKV_H_ */

@@ -1,0 +1,310 @@
+"""GPU parity of the pooled (P <= 16, D = 128) path against the CPU oracle.
+
+Source: vLLM page "kpool_compress" (_kpool_decode_update_batched_kernel,
+_kpool_softmax_rotate_write_cache_kernel, _kpool_tail_seed_kernel).  Every
+call goes through the C ABI (libckv.so) via the ctypes binding.
+
+Bit-exactness is checked stage by stage (the oracle's rotation fed the GPU's
+bf16 row must give the GPU's rotated row; the oracle's quantiser fed that
+must give the GPU's codes and scale) and end to end (rows whose bf16 pooled
+value agrees are identical; the pooled fp32 value is within tolerance).
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import (assert_close_rel, assert_fp8_within_one, bf16_bits, cache_rows, f32, u8)
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+
+
+@pytest.fixture(scope="module")
+def ck():
+    import compressed_kv_attention_gated_gb300 as ck
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ck.load()
+    return ck
+
+
+def _to(d, dev):
+    return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def check_rows(ora, gpu_x, gpu_xb, gpu_yb, gpu_q, gpu_s, ref, round_scale, what):
+    """Stage-wise and end-to-end comparison of pooled rows."""
+    assert_close_rel(gpu_x, ref["x"], what + " x")
+    np.testing.assert_array_equal(ora.rotate_bf16(gpu_xb), gpu_yb, err_msg=what + " rotation stage")
+    q2, s2 = ora.quantize_rows(gpu_yb, round_scale)
+    np.testing.assert_array_equal(q2, gpu_q, err_msg=what + " quant stage codes")
+    np.testing.assert_array_equal(s2.view(np.uint32), gpu_s.view(np.uint32), err_msg=what + " quant stage scales")
+    same = np.all(gpu_xb == ref["xb"], axis=1)
+    np.testing.assert_array_equal(gpu_q[same], ref["q"][same], err_msg=what + " codes (same xb rows)")
+    np.testing.assert_array_equal(gpu_s[same].view(np.uint32), ref["scale"][same].view(np.uint32))
+    # rows whose bf16 rounding of x landed on the other neighbour: one bf16 step at most
+    diff = ~same
+    if diff.any():
+        a = gpu_xb[diff].astype(np.int32)
+        b = ref["xb"][diff].astype(np.int32)
+        assert np.all(np.abs(a - b) <= 1) or np.all(np.abs(np.abs(a) - np.abs(b)) <= 1), what
+    same_scale = gpu_s == ref["scale"]
+    assert_fp8_within_one(gpu_q[same_scale], ref["q"][same_scale], what + " codes")
+    return int(diff.sum())
+
+
+# ------------------------------------------------------------------ one-shot
+@pytest.mark.parametrize("P", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("round_scale", [True, False])
+def test_kpool_compress_vs_oracle(ck, ora, P, round_scale):
+    from compressed_kv_attention_gated_gb300 import synth
+
+    n = 203  # several CTAs of 8 pools and a ragged tail
+    g = torch.Generator().manual_seed(100 + P)
+    slot_k = (torch.randn((n, P, D), generator=g)).to(torch.bfloat16)
+    slot_s = (torch.randn((n, P, D), generator=g) * 2).to(torch.bfloat16)
+    ape = (torch.randn((P, D), generator=g) * 0.1)
+    ps = 64
+    pages = (n + ps - 1) // ps + 1
+    loc = torch.randperm(pages * ps, generator=g)[:n].to(torch.int64)
+    cache0 = torch.full((pages, ps, D + 4), 0x5A, dtype=torch.uint8)
+    dev = "cuda"
+    cache = cache0.to(dev)
+    out_q = torch.zeros((n, D), dtype=torch.uint8, device=dev)
+    out_s = torch.zeros((n,), dtype=torch.float32, device=dev)
+    tx = torch.zeros((n, D), dtype=torch.float32, device=dev)
+    txb = torch.zeros((n, D), dtype=torch.bfloat16, device=dev)
+    tyb = torch.zeros((n, D), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros((1,), dtype=torch.int32, device=dev)
+    ck.ckv_kpool_compress(slot_k.to(dev), slot_s.to(dev), ape.to(dev), kv_cache=cache, loc=loc.to(dev),
+                          out_fp8=out_q, out_scale=out_s, round_scale=round_scale, tap_x=tx, tap_xb=txb,
+                          tap_yb=tyb, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref_cache = u8(cache0).copy()
+    ref = ora.kpool_compress(ref_cache, ps, bf16_bits(slot_k), bf16_bits(slot_s), f32(ape), loc.numpy(),
+                             return_compressed=True, round_scale=round_scale, taps=True)
+    gq, gs = u8(out_q), f32(out_s)
+    check_rows(ora, f32(tx), bf16_bits(txb), bf16_bits(tyb), gq, gs, ref, round_scale, f"P={P}")
+    # the cache holds the same rows at loc, and nothing else changed
+    gcache = u8(cache)
+    cq, cs = cache_rows(gcache, ps, D, loc.numpy())
+    np.testing.assert_array_equal(cq, gq)
+    np.testing.assert_array_equal(cs.view(np.uint32), gs.view(np.uint32))
+    rq, rs = cache_rows(ref_cache, ps, D, loc.numpy())
+    mask = np.ones(gcache.size, bool)
+    flat = np.arange(gcache.size).reshape(gcache.shape)
+    for l in loc.numpy():
+        page, tok = divmod(int(l), ps)
+        base = page * ps * (D + 4)
+        mask[base + tok * D: base + tok * D + D] = False
+        mask[base + ps * D + 4 * tok: base + ps * D + 4 * tok + 4] = False
+    assert np.all(gcache.reshape(-1)[mask] == 0x5A), "bytes outside the written rows changed"
+
+
+def test_kpool_compress_write_mask_and_cache_only(ck, ora):
+    n, P = 77, 16
+    g = torch.Generator().manual_seed(7)
+    slot_k = torch.randn((n, P, D), generator=g).to(torch.bfloat16)
+    slot_s = torch.randn((n, P, D), generator=g).to(torch.bfloat16)
+    ape = torch.randn((P, D), generator=g) * 0.1
+    wm = torch.rand((n,), generator=g) < 0.6
+    ps = 16
+    pages = (n + ps - 1) // ps
+    loc = torch.arange(n, dtype=torch.int64)
+    cache0 = torch.full((pages, ps, D + 4), 0xC3, dtype=torch.uint8)
+    cache = cache0.cuda()
+    ck.ckv_kpool_compress(slot_k.cuda(), slot_s.cuda(), ape.cuda(), kv_cache=cache, loc=loc.cuda(),
+                          write_mask=wm.cuda())
+    torch.cuda.synchronize()
+    ref_cache = u8(cache0).copy()
+    ora.kpool_compress(ref_cache, ps, bf16_bits(slot_k), bf16_bits(slot_s), f32(ape), loc.numpy(),
+                       write_mask=wm.numpy().astype(np.uint8))
+    g_cache = u8(cache)
+    gq, gs = cache_rows(g_cache, ps, D, loc.numpy())
+    rq, rs = cache_rows(ref_cache, ps, D, loc.numpy())
+    w = wm.numpy()
+    assert np.all(gq[~w] == 0xC3)
+    same_s = gs[w] == rs[w]
+    assert same_s.mean() > 0.97
+    assert_fp8_within_one(gq[w][same_s], rq[w][same_s], "masked compress")
+
+
+def test_kpool_compress_bad_loc_flags_and_skips(ck):
+    n, P = 16, 16
+    slot = torch.randn((n, P, D), device="cuda").to(torch.bfloat16)
+    ape = torch.zeros((P, D), device="cuda")
+    ps = 16
+    cache = torch.full((1, ps, D + 4), 7, dtype=torch.uint8, device="cuda")
+    loc = torch.arange(n, dtype=torch.int64, device="cuda")
+    loc[3] = ps  # one past the end
+    loc[5] = -2
+    err = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    ck.ckv_kpool_compress(slot, slot, ape, kv_cache=cache, loc=loc, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 0x4
+    c = u8(cache).reshape(-1)
+    assert np.all(c[3 * D:4 * D] == 7) and np.all(c[5 * D:6 * D] == 7)
+    assert not np.all(c[4 * D:5 * D] == 7)
+
+
+# -------------------------------------------------------------- decode update
+def _run_decode(ck, d, round_scale, taps=True):
+    dev = "cuda"
+    B, N = d["B"], d["N"]
+    cache = d["kv_cache"].to(dev)
+    ring = d["ring"].to(dev)
+    tx = torch.full((B * N, D), float("nan"), device=dev) if taps else None
+    txb = torch.zeros((B * N, D), dtype=torch.bfloat16, device=dev) if taps else None
+    tyb = torch.zeros((B * N, D), dtype=torch.bfloat16, device=dev) if taps else None
+    err = torch.zeros((1,), dtype=torch.int32, device=dev)
+    ck.ckv_kpool_decode_update(cache, ring, d["tail_slot_mapping"].to(dev), d["slot_mapping"].to(dev),
+                               d["positions"].to(dev), d["key"].to(dev), d["score"].to(dev), d["ape"].to(dev),
+                               round_scale=round_scale, tap_x=tx, tap_xb=txb, tap_yb=tyb, err_word=err)
+    torch.cuda.synchronize()
+    return cache, ring, tx, txb, tyb, int(err.item())
+
+
+def _oracle_decode(ora, d, round_scale):
+    cache = u8(d["kv_cache"]).copy()
+    ring = bf16_bits(d["ring"]).copy()
+    ref = ora.kpool_decode_update(cache, d["page_size"], ring, d["tail_slot_mapping"].cpu().numpy(),
+                                  d["slot_mapping"].cpu().numpy(), d["positions"].cpu().numpy(),
+                                  bf16_bits(d["key"]), bf16_bits(d["score"]), f32(d["ape"]),
+                                  round_scale=round_scale, taps=True)
+    return cache, ring, ref
+
+
+def _compare_decode(ora, d, gpu, oref, round_scale, what):
+    cache, ring, tx, txb, tyb, err = gpu
+    rcache, rring, ref = oref
+    assert err == 0
+    np.testing.assert_array_equal(bf16_bits(ring), rring, err_msg=what + " ring")
+    sm = d["slot_mapping"].cpu().numpy().reshape(-1)
+    pos = d["positions"].cpu().numpy().reshape(-1)
+    P = d["P"]
+    closing = np.nonzero((sm >= 0) & (pos >= 0) & (pos % P == P - 1))[0]
+    assert len(closing) > 0
+    gq, gs = cache_rows(u8(cache), d["page_size"], D, sm[closing])
+    sub = {k: v[closing] for k, v in ref.items()}
+    rq, rs = cache_rows(rcache, d["page_size"], D, sm[closing])
+    sub["q"], sub["scale"] = rq, rs
+    ndiff = check_rows(ora, f32(tx)[closing], bf16_bits(txb)[closing], bf16_bits(tyb)[closing], gq, gs, sub,
+                       round_scale, what)
+    # everything but the closing rows is untouched on both sides
+    g = u8(cache).reshape(-1).copy()
+    r = rcache.reshape(-1).copy()
+    ps = d["page_size"]
+    for l in sm[closing]:
+        page, tok = divmod(int(l), ps)
+        base = page * ps * (D + 4)
+        for arr in (g, r):
+            arr[base + tok * D: base + tok * D + D] = 0
+            arr[base + ps * D + 4 * tok: base + ps * D + 4 * tok + 4] = 0
+    np.testing.assert_array_equal(g, r, err_msg=what + " untouched cache bytes")
+    return len(closing), ndiff
+
+
+@pytest.mark.parametrize("round_scale", [True, False])
+def test_kpool_decode_tiny_in_order_matches_oracle_and_one_shot(ck, ora, round_scale):
+    from compressed_kv_attention_gated_gb300 import synth
+
+    d = synth.tiny_pooled("cpu", seed=0)
+    gpu = _run_decode(ck, d, round_scale)
+    oref = _oracle_decode(ora, d, round_scale)
+    n, _ = _compare_decode(ora, d, gpu, oref, round_scale, "tiny decode")
+    assert n == 16
+    # the same 16 pools through the one-shot kernel give bit-identical cache rows
+    cache2 = d["kv_cache"].cuda()
+    ck.ckv_kpool_compress(d["slot_k"].cuda(), d["slot_score"].cuda(), d["ape"].cuda(), kv_cache=cache2,
+                          loc=d["loc"].cuda(), round_scale=round_scale)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(u8(cache2), u8(gpu[0]))
+
+
+@pytest.mark.parametrize("round_scale", [True, False])
+def test_kpool_decode_verify_batch_full_size(ck, ora, round_scale):
+    """512 requests x 4 verify tokens, prefilled ring, 5% padding (full size)."""
+    from compressed_kv_attention_gated_gb300 import synth
+
+    d = synth.pooled_decode("cpu", seed=0 if round_scale else 1)
+    gpu = _run_decode(ck, d, round_scale)
+    oref = _oracle_decode(ora, d, round_scale)
+    n, ndiff = _compare_decode(ora, d, gpu, oref, round_scale, "decode/verify")
+    assert n > 50
+    assert ndiff <= max(2, n // 20)
+
+
+@pytest.mark.parametrize("P", [1, 4, 16])
+def test_kpool_decode_long_sequences_and_across_calls(ck, ora, P):
+    """N > P tokens per call (several closings per request) and a pool that is
+    filled over several calls: the ring carries the stashes between calls."""
+    from compressed_kv_attention_gated_gb300 import synth
+
+    B, total = 5, 3 * P + 5
+    d = synth.tiny_pooled("cpu", seed=3, B=B, N=total, P=P)
+    # shuffle tail blocks so requests do not own block b
+    perm = torch.randperm(B, generator=torch.Generator().manual_seed(1))
+    pos = d["positions"].to(torch.int64)
+    d["tail_slot_mapping"] = (perm[:, None] * P + pos % P).to(torch.int32)
+    ring_g = d["ring"].cuda()
+    cache_g = d["kv_cache"].cuda()
+    rcache = u8(d["kv_cache"]).copy()
+    rring = bf16_bits(d["ring"]).copy()
+    cuts = [0, 1, P + 2, total]
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        sl = {k: d[k][:, a:b].contiguous() for k in ("tail_slot_mapping", "slot_mapping", "positions", "key", "score")}
+        ck.ckv_kpool_decode_update(cache_g, ring_g, sl["tail_slot_mapping"].cuda(), sl["slot_mapping"].cuda(),
+                                   sl["positions"].cuda(), sl["key"].cuda(), sl["score"].cuda(), d["ape"].cuda())
+        ora.kpool_decode_update(rcache, d["page_size"], rring, sl["tail_slot_mapping"].numpy(),
+                                sl["slot_mapping"].numpy(), sl["positions"].numpy(), bf16_bits(sl["key"]),
+                                bf16_bits(sl["score"]), f32(d["ape"]))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bf16_bits(ring_g), rring)
+    sm = d["slot_mapping"].numpy().reshape(-1)
+    locs = sm[sm >= 0]
+    gq, gs = cache_rows(u8(cache_g), d["page_size"], D, locs)
+    rq, rs = cache_rows(rcache, d["page_size"], D, locs)
+    same = gs == rs
+    assert same.mean() > 0.9
+    assert_fp8_within_one(gq[same], rq[same], "across calls")
+
+
+def test_kpool_decode_bad_block_flags(ck):
+    B, N, P = 2, 1, 16
+    ring = torch.zeros((1, 2, P, D), dtype=torch.bfloat16, device="cuda")
+    cache = torch.zeros((1, 16, D + 4), dtype=torch.uint8, device="cuda")
+    tsm = torch.tensor([[5 * P + 3], [0 * P + 4]], dtype=torch.int32, device="cuda")  # block 5 does not exist
+    sm = torch.full((B, N), -1, dtype=torch.int32, device="cuda")
+    pos = torch.tensor([[3], [4]], dtype=torch.int32, device="cuda")
+    key = torch.ones((B, N, D), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    ck.ckv_kpool_decode_update(cache, ring, tsm, sm, pos, key, key, torch.zeros((P, D), device="cuda"), err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 0x2
+    r = bf16_bits(ring)
+    assert np.all(r[0, 0, 4] == 0x3F80) and np.all(r[0, 0, 3] == 0)
+
+
+def test_kpool_seed_tail_vs_oracle(ck, ora):
+    P = 16
+    lens = [37, 5, 16, 0, 130]
+    g = torch.Generator().manual_seed(5)
+    blocks = torch.randperm(len(lens), generator=g)
+    ts = []
+    for r, n in enumerate(lens):
+        ts.append(blocks[r] * P + torch.arange(n) % P)
+    tslot = torch.cat(ts).to(torch.int32)
+    tslot[7] = -1  # a padded entry
+    n = tslot.numel()
+    key = torch.randn((n, D), generator=g).to(torch.bfloat16)
+    score = torch.randn((n, D), generator=g).to(torch.bfloat16)
+    ring0 = torch.randn((len(lens), 2, P, D), generator=g).to(torch.bfloat16)
+    ring = ring0.cuda()
+    ck.ckv_kpool_seed_tail(ring, key.cuda(), score.cuda(), tslot.cuda())
+    torch.cuda.synchronize()
+    rring = bf16_bits(ring0).copy()
+    ora.kpool_seed_tail(rring, bf16_bits(key), bf16_bits(score), tslot.numpy())
+    np.testing.assert_array_equal(bf16_bits(ring), rring)
