@@ -318,7 +318,7 @@ class HostIO:
         ck = s.ck
         for key, d in (("cp", s.cp), ("lc", s.lc)):
             hc, hw = self.plan_host[key]
-            c, nc, w, nw = ck.ckv_plan_online_prefill(d["seq_lens"], d["extend_lens"], compress_plan=hc, write_plan=hw)
+            _, _, nc, nw = ck.ckv_plan_online_prefill(d["seq_lens"], d["extend_lens"], compress_plan=hc, write_plan=hw)
             dc, _, dw, _ = s.plans[key][:4]
             if nc:
                 dc[:nc].copy_(hc[:nc], non_blocking=True)
