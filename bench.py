@@ -549,7 +549,15 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-variant", type=int, default=0,
+                    help="compress-pass kernel: 0 auto, 1 one CTA per segment, 2 TMA pipeline")
     args = ap.parse_args()
+    if args.impl == "ours":
+        import compressed_kv_attention_gated_gb300 as ck
+        from compressed_kv_attention_gated_gb300 import build as libbuild
+
+        libbuild.build()
+        ck.ckv_c128_prefill_set_variant(args.prefill_variant)
     if args.case:
         run_case(args)
         return

@@ -32,7 +32,8 @@ _STATUS_FUNCS = {
     "ckv_c128_online_prefill": 18,
     "ckv_plan_online_prefill": 9,
 }
-EXPORTED = tuple(_STATUS_FUNCS) + ("ckv_status_string", "ckv_last_cuda_error", "ckv_abi_version")
+EXPORTED = tuple(_STATUS_FUNCS) + ("ckv_status_string", "ckv_last_cuda_error", "ckv_abi_version",
+                                    "ckv_c128_prefill_set_variant")
 
 
 class CkvError(RuntimeError):
@@ -94,6 +95,8 @@ def load():
             L.ckv_last_cuda_error.argtypes = []
             L.ckv_abi_version.restype = ctypes.c_int32
             L.ckv_abi_version.argtypes = []
+            L.ckv_c128_prefill_set_variant.restype = ctypes.c_int32
+            L.ckv_c128_prefill_set_variant.argtypes = [ctypes.c_int32]
             _lib = L
     return _lib
 
@@ -275,6 +278,16 @@ def ckv_c128_online_prefill(state, input, out, ape, indices, compress_plan, num_
         _ptr(state), state.numel() // (3 * D), _ptr(input), _dtype(input), T, _ptr(out), _ptr(ape),
         _ptr(indices), _ptr(load_indices), B, _ptr(compress_plan), int(num_compress), _ptr(write_plan),
         int(num_write), D, int(bool(use_pdl)), _ptr(err_word), _stream(stream, input)))
+
+
+def ckv_c128_prefill_set_variant(variant: int) -> int:
+    """Select the compress-pass kernel (0 auto, 1 one CTA per segment, 2 TMA pipeline).
+
+    Returns the previous setting; raises on an unknown value."""
+    prev = load().ckv_c128_prefill_set_variant(int(variant))
+    if prev < 0:
+        raise ValueError(f"unknown prefill variant {variant}")
+    return prev
 
 
 def ckv_plan_online_prefill(seq_lens, extend_lens, num_tokens=None, pad_for_graph=False,

@@ -18,6 +18,8 @@
 //              segment starts mid-chunk, then stored.  Compress and write
 //              passes are two launches in stream order (optionally chained
 //              by programmatic dependent launch).
+#include <type_traits>
+
 #include "ckv_device.cuh"
 #include "ckv_launch.h"
 
@@ -268,13 +270,24 @@ cudaError_t decode_d(const C128DecodeArgs& a, bool use_pdl, cudaStream_t s) {
   return launch(c128_decode_kernel<D, InT>, grid, dim3(kDecodeWarps * 32), use_pdl, s, a);
 }
 
+constexpr uint32_t kTmaMinSegments = 32;
+
 template <int D, typename InT>
 cudaError_t prefill_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
   constexpr int S = D / 128;
+  constexpr int dtype = std::is_same<InT, float>::value ? CKV_F32 : CKV_BF16;
   if (a.num_compress) {
-    const dim3 grid(static_cast<unsigned>(a.num_compress) * S);
-    cudaError_t e = launch(c128_prefill_kernel<D, InT, false>, grid, dim3(kPrefillWarps * 32),
-                           use_pdl, s, a);
+    const int v = prefill_variant();
+    cudaError_t e = cudaErrorNotSupported;
+    if (v != 1 && (v == 2 || a.num_compress >= kTmaMinSegments) &&
+        c128_prefill_tma_supported(a, D, dtype)) {
+      e = launch_c128_prefill_compress_tma(a, D, dtype, use_pdl, s);
+      if (e == cudaErrorNotSupported) (void)cudaGetLastError();
+    }
+    if (e == cudaErrorNotSupported) {
+      const dim3 grid(static_cast<unsigned>(a.num_compress) * S);
+      e = launch(c128_prefill_kernel<D, InT, false>, grid, dim3(kPrefillWarps * 32), use_pdl, s, a);
+    }
     if (e != cudaSuccess) return e;
   }
   if (a.num_write) {

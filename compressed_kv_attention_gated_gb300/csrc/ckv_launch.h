@@ -100,6 +100,13 @@ cudaError_t launch_c128_decode(const C128DecodeArgs& a, int D, int in_dtype, boo
 cudaError_t launch_c128_prefill(const C128PrefillArgs& a, int D, int in_dtype, bool use_pdl,
                                 cudaStream_t s);
 
+// TMA-pipelined compress pass (prefill_tma.cu).
+bool c128_prefill_tma_supported(const C128PrefillArgs& a, int D, int in_dtype);
+cudaError_t launch_c128_prefill_compress_tma(const C128PrefillArgs& a, int D, int in_dtype,
+                                             bool use_pdl, cudaStream_t s);
+// 0 auto, 1 one CTA per segment, 2 TMA pipeline (capi.cu).
+int prefill_variant();
+
 // Host planner (planner.cpp).
 ckv_status plan_online_prefill_host(const int64_t* seq_lens, const int64_t* extend_lens,
                                     uint32_t B, uint32_t num_tokens,

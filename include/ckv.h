@@ -59,6 +59,7 @@ typedef int32_t ckv_status;
 #define CKV_DEVERR_CACHE_LOC 0x4u  /* cache location outside [0, num_pages * page_size) */
 #define CKV_DEVERR_PLAN 0x8u       /* plan entry fields inconsistent or out of range */
 #define CKV_DEVERR_SEQ_LEN 0x10u   /* decode seq_len < 1 */
+#define CKV_DEVERR_TIMEOUT 0x20u   /* a pipeline wait gave up after 2 s (never expected) */
 
 typedef int32_t ckv_dtype;
 #define CKV_F32 0
@@ -225,6 +226,17 @@ ckv_status ckv_c128_online_prefill(float* state, int64_t num_slots, const void* 
                                    const ckv_plan_entry* compress_plan, uint32_t num_compress,
                                    const ckv_plan_entry* write_plan, uint32_t num_write, int32_t D,
                                    int32_t use_pdl, int32_t* err_word, void* stream);
+
+/*
+ * Kernel choice for the compress pass of ckv_c128_online_prefill (process-wide).
+ *   0 = automatic (default): the TMA-pipelined persistent kernel when there are
+ *       at least 32 compress segments, otherwise the one-CTA-per-segment kernel;
+ *   1 = always the one-CTA-per-segment kernel;
+ *   2 = always the TMA-pipelined kernel (when the device supports it).
+ * Both compute the same function.  Returns the previous setting, or -1 (and
+ * changes nothing) for an unknown value.
+ */
+int32_t ckv_c128_prefill_set_variant(int32_t variant);
 
 /*
  * Host planner for the online c128 prefill (sglang c128_online.cuh page,

@@ -29,6 +29,14 @@ def ck():
     return ck
 
 
+@pytest.fixture(params=[1, 2], ids=["cta_per_segment", "tma_pipeline"])
+def variant(request, ck):
+    """Run a prefill test with each compress-pass kernel."""
+    prev = ck.ckv_c128_prefill_set_variant(request.param)
+    yield request.param
+    ck.ckv_c128_prefill_set_variant(prev)
+
+
 def _np_input(t):
     return bf16_bits(t) if t.dtype == torch.bfloat16 else f32(t)
 
@@ -176,7 +184,7 @@ def test_planner_matches_oracle_segmenter(ck, ora):
 
 @pytest.mark.parametrize("D", [128, 256, 512])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_c128_prefill_small(ck, ora, D, dtype):
+def test_c128_prefill_small(variant, ck, ora, D, dtype):
     from compressed_kv_attention_gated_gb300 import synth
 
     d = synth.c128_prefill("cpu", seed=D + (dtype == torch.bfloat16), B=9, D=D, max_prefix=500,
@@ -189,7 +197,7 @@ def test_c128_prefill_small(ck, ora, D, dtype):
 
 @pytest.mark.parametrize("use_pdl", [False, True])
 @pytest.mark.parametrize("pad", [False, True])
-def test_c128_prefill_full_size(ck, ora, use_pdl, pad):
+def test_c128_prefill_full_size(variant, ck, ora, use_pdl, pad):
     """64 requests, prefix U[0,16384], extend U[1,8192], D=512 fp32 (about 262K tokens)."""
     from compressed_kv_attention_gated_gb300 import synth
 
@@ -200,7 +208,7 @@ def test_c128_prefill_full_size(ck, ora, use_pdl, pad):
     assert nrows > 1000 and nstates > 30
 
 
-def test_c128_prefill_load_indices_differ(ck, ora):
+def test_c128_prefill_load_indices_differ(variant, ck, ora):
     from compressed_kv_attention_gated_gb300 import synth
 
     d = synth.c128_prefill("cpu", seed=11, B=12, D=256, max_prefix=400, max_extend=300, num_slots=40)
@@ -213,7 +221,7 @@ def test_c128_prefill_load_indices_differ(ck, ora):
     _check_prefill(ora, d, g_state, g_out, load_indices=lidx)
 
 
-def test_c128_prefill_then_decode_then_prefill(ck, ora):
+def test_c128_prefill_then_decode_then_prefill(variant, ck, ora):
     """A sequence fed through prefill, decode steps and another prefill equals the
     oracle's chain (the running state is the only carried checkpoint)."""
     from compressed_kv_attention_gated_gb300 import synth
@@ -261,7 +269,7 @@ def test_c128_prefill_then_decode_then_prefill(ck, ora):
         assert_close_rel(gs[live, 2], state_o[live, 2], f"state kv after step {step}")
 
 
-def test_c128_prefill_sentinels_and_bad_plans(ck):
+def test_c128_prefill_sentinels_and_bad_plans(variant, ck):
     D = 128
     T = 300
     state = torch.zeros((2, 3, D), device="cuda")
