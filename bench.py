@@ -52,9 +52,16 @@ WORKLOAD = ("serving step: pooled decode/verify B=512 N=4 P=16 D=128 + c128 deco
             "c128 prefill 64 req (prefix U[0,16384], extend U[1,8192]) D=512 fp32 + long-context prefill "
             "8x131072 D=512 bf16 (Student-t scores) + pooled one-shot 65536 pools P=16 D=128 bf16")
 
-# DRAM traffic per launch of the dominant kernel from one ncu capture (see
-# profiles/); `src` pins the kernel source it was taken on.
-NCU_TRAFFIC = {}
+# DRAM traffic (read + write bytes) per launch of the dominant kernel from one
+# ncu capture of a 131,072-token case, scaled by tokens to the 8 x 131,072-token
+# launch (profiles/c128_prefill_tma_kernel_bf16_d512_131072tok.md); `src` is a
+# hash of the kernel's source files at capture time: any later change to them
+# turns the figure into null.
+NCU_TRAFFIC = {
+    "c128_online_prefill_bf16": {"bytes_per_launch": 2186.6e6, "files": ["prefill_tma.cu", "ckv_tma.cuh",
+                                                                         "ckv_device.cuh"],
+                                 "src": "aa4183fc8e3323a1"},
+}
 
 
 # ------------------------------------------------------------------ helpers
@@ -68,11 +75,11 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def _src_hash():
+def _src_hash(files):
     import hashlib
 
     h = hashlib.sha256()
-    for f in ("c128.cu", "kpool.cu", "ckv_device.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "compressed_kv_attention_gated_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -614,7 +621,7 @@ def main():
     dom = max(range(nk), key=lambda i: per_kernel_ms[i])
     dom_gbs = step.bytes[dom] / (per_kernel_ms[dom] / 1e3) / 1e9
     tr = NCU_TRAFFIC.get(step.names[dom])
-    traffic = tr["bytes_per_launch"] if tr and tr.get("src") == _src_hash() else None
+    traffic = tr["bytes_per_launch"] if tr and tr.get("src") == _src_hash(tr["files"]) else None
     roofline = {"bound": "hbm", "kernel": step.names[dom], "achieved": round(dom_gbs, 1), "peak": peak,
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dom_gbs / peak, 4), "traffic": traffic,
                 "algorithmic_bytes_per_launch": int(step.bytes[dom]), "unit_bytes": step.units[step.names[dom]]}

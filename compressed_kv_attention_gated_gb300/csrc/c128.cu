@@ -41,6 +41,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   const int b = blockIdx.x * kDecodeWarps + (threadIdx.x >> 5);
   if (b >= a.B) return;
 
+  // The slot index gates the dependent state loads: issue it before the input stream.
+  const int32_t index = a.indices[b];
+  const int32_t seq_len = a.seq_lens[b];
   const InT* in = static_cast<const InT*>(a.input) + static_cast<int64_t>(b) * 2 * D;
   float4 kin[C], sin_[C];
 #pragma unroll
@@ -48,8 +51,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     kin[c] = In4<InT>::load(in, 4 * lane + 128 * c);
     sin_[c] = In4<InT>::load(in + D, 4 * lane + 128 * c);
   }
-  const int32_t index = a.indices[b];
-  const int32_t seq_len = a.seq_lens[b];
   if (seq_len < 1) {
     if (lane == 0) flag_error(a.err, CKV_DEVERR_SEQ_LEN);
     return;
@@ -279,8 +280,11 @@ cudaError_t prefill_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
   if (a.num_compress) {
     const int v = prefill_variant();
     cudaError_t e = cudaErrorNotSupported;
-    if (v != 1 && (v == 2 || a.num_compress >= kTmaMinSegments) &&
-        c128_prefill_tma_supported(a, D, dtype)) {
+    // Automatic choice: the TMA pipeline for bf16 inputs with enough segments to
+    // amortise its per-CTA set-up; fp32 inputs measured faster on one CTA per
+    // segment (16-byte vector loads of 128-channel slices).
+    const bool tma = v == 2 || (v == 0 && dtype == CKV_BF16 && a.num_compress >= kTmaMinSegments);
+    if (tma && c128_prefill_tma_supported(a, D, dtype)) {
       e = launch_c128_prefill_compress_tma(a, D, dtype, use_pdl, s);
       if (e == cudaErrorNotSupported) (void)cudaGetLastError();
     }
