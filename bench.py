@@ -558,6 +558,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-variant", type=int, default=0,
                     help="compress-pass kernel: 0 auto, 1 one CTA per segment, 2 TMA pipeline")
+    ap.add_argument("--kpool-variant", type=int, default=0,
+                    help="pooled one-shot kernel: 0 auto, 1 one warp per pool, 2 bulk-copy pipeline")
     args = ap.parse_args()
     if args.impl == "ours":
         import compressed_kv_attention_gated_gb300 as ck
@@ -565,6 +567,7 @@ def main():
 
         libbuild.build()
         ck.ckv_c128_prefill_set_variant(args.prefill_variant)
+        ck.ckv_kpool_compress_set_variant(args.kpool_variant)
     if args.case:
         run_case(args)
         return

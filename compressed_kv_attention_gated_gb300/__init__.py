@@ -10,6 +10,7 @@ from .ckv import (  # noqa: F401
     ckv_c128_online_prefill,
     ckv_c128_prefill_set_variant,
     ckv_kpool_compress,
+    ckv_kpool_compress_set_variant,
     ckv_kpool_decode_update,
     ckv_kpool_seed_tail,
     ckv_plan_online_prefill,

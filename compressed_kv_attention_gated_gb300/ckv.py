@@ -33,7 +33,7 @@ _STATUS_FUNCS = {
     "ckv_plan_online_prefill": 9,
 }
 EXPORTED = tuple(_STATUS_FUNCS) + ("ckv_status_string", "ckv_last_cuda_error", "ckv_abi_version",
-                                    "ckv_c128_prefill_set_variant")
+                                    "ckv_c128_prefill_set_variant", "ckv_kpool_compress_set_variant")
 
 
 class CkvError(RuntimeError):
@@ -95,8 +95,9 @@ def load():
             L.ckv_last_cuda_error.argtypes = []
             L.ckv_abi_version.restype = ctypes.c_int32
             L.ckv_abi_version.argtypes = []
-            L.ckv_c128_prefill_set_variant.restype = ctypes.c_int32
-            L.ckv_c128_prefill_set_variant.argtypes = [ctypes.c_int32]
+            for fn in (L.ckv_c128_prefill_set_variant, L.ckv_kpool_compress_set_variant):
+                fn.restype = ctypes.c_int32
+                fn.argtypes = [ctypes.c_int32]
             _lib = L
     return _lib
 
@@ -287,6 +288,16 @@ def ckv_c128_prefill_set_variant(variant: int) -> int:
     prev = load().ckv_c128_prefill_set_variant(int(variant))
     if prev < 0:
         raise ValueError(f"unknown prefill variant {variant}")
+    return prev
+
+
+def ckv_kpool_compress_set_variant(variant: int) -> int:
+    """Select the pooled one-shot kernel (0 auto, 1 one warp per pool, 2 bulk-copy pipeline).
+
+    Returns the previous setting; raises on an unknown value."""
+    prev = load().ckv_kpool_compress_set_variant(int(variant))
+    if prev < 0:
+        raise ValueError(f"unknown kpool compress variant {variant}")
     return prev
 
 

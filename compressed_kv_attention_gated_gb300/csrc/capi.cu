@@ -13,6 +13,7 @@ namespace {
 
 thread_local int32_t g_last_cuda_error = 0;
 std::atomic<int32_t> g_prefill_variant{0};
+std::atomic<int32_t> g_kpool_compress_variant{0};
 
 ckv_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return CKV_OK;
@@ -28,6 +29,7 @@ bool head_dim_ok(int32_t D) { return D == 128 || D == 256 || D == 512; }
 
 namespace ckv {
 int prefill_variant() { return g_prefill_variant.load(std::memory_order_relaxed); }
+int kpool_compress_variant() { return g_kpool_compress_variant.load(std::memory_order_relaxed); }
 }  // namespace ckv
 
 extern "C" {
@@ -35,6 +37,11 @@ extern "C" {
 int32_t ckv_c128_prefill_set_variant(int32_t variant) {
   if (variant < 0 || variant > 2) return -1;
   return g_prefill_variant.exchange(variant);
+}
+
+int32_t ckv_kpool_compress_set_variant(int32_t variant) {
+  if (variant < 0 || variant > 2) return -1;
+  return g_kpool_compress_variant.exchange(variant);
 }
 
 int32_t ckv_abi_version(void) { return 1; }

@@ -106,6 +106,8 @@ cudaError_t launch_c128_prefill_compress_tma(const C128PrefillArgs& a, int D, in
                                              bool use_pdl, cudaStream_t s);
 // 0 auto, 1 one CTA per segment, 2 TMA pipeline (capi.cu).
 int prefill_variant();
+// 0 auto, 1 one warp per pool, 2 persistent bulk-copy pipeline (capi.cu).
+int kpool_compress_variant();
 
 // Host planner (planner.cpp).
 ckv_status plan_online_prefill_host(const int64_t* seq_lens, const int64_t* extend_lens,

@@ -13,6 +13,10 @@
 //     per CTA;
 //   * exact two-pass softmax from registers: z = score + ape for the P slots,
 //     max, then one ex2 per element;
+//   * for large batches, a persistent variant in which every warp streams its
+//     pools through a private two-stage ring of shared-memory buffers with 1-D
+//     bulk copies (cp.async.bulk, completion on an mbarrier), so the next
+//     pool's 8 KB arrive while the current one is reduced, rotated and packed;
 //   * Hadamard-128: two butterfly spans inside the lane (1, 2), then five
 //     warp-shuffle spans (4..64 = lane masks 1..16), ascending; warp-shuffle
 //     absmax; fused FP8-e4m3 packing (cvt.rn.satfinite) and cache write.
@@ -20,6 +24,7 @@
 // The pooled path is memory bound (no dense contraction); no tensor cores.
 #include "ckv_device.cuh"
 #include "ckv_launch.h"
+#include "ckv_tma.cuh"
 
 namespace ckv {
 namespace {
@@ -189,6 +194,116 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   write_taps(a.tap_x, a.tap_xb, a.tap_yb, pool, lane, x, xb, yb);
 }
 
+// One-shot pooled compression, persistent and bulk-copy fed.  Warp g (of W in
+// the grid) handles pools g, g + W, g + 2W, ...; each pool's P key rows and P
+// score rows (contiguous, P * 256 B each) are copied into one of the warp's
+// kBulkStages shared-memory stages by lane 0, and the whole warp waits on the
+// stage's mbarrier before reading it.  Pools masked out by write_mask are
+// neither copied nor computed.  Waits are bounded; a timeout flags
+// CKV_DEVERR_TIMEOUT, drains the warp's own copies and leaves.
+constexpr int kBulkWarps = 12;
+constexpr int kBulkStages = 2;
+
+template <int P>
+struct BulkLayout {
+  static constexpr int kPoolBytes = P * kD * 2;  // one array of one pool
+  static constexpr int kApe = 0;
+  static constexpr int kBuf = P * kD * 4;
+  static constexpr int kBar = kBuf + kBulkWarps * kBulkStages * 2 * kPoolBytes;
+  static constexpr int kBytes = kBar + kBulkWarps * kBulkStages * 8;
+};
+
+template <int P, bool kRound>
+__global__ void __launch_bounds__(kBulkWarps * 32, 1)
+    kpool_compress_bulk_kernel(const __grid_constant__ KpoolCompressArgs a) {
+  using L = BulkLayout<P>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* s_ape = reinterpret_cast<float*>(smem + L::kApe);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* mybuf = smem + L::kBuf + warp * kBulkStages * 2 * L::kPoolBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar) + warp * kBulkStages;
+  if (lane == 0) {
+    for (int s = 0; s < kBulkStages; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  stage_ape<P>(s_ape, a.ape);  // ends with __syncthreads()
+
+  const int64_t W = static_cast<int64_t>(gridDim.x) * kBulkWarps;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kBulkWarps + warp;
+  auto wanted = [&](int64_t pool) { return pool < a.n_pools && (!a.write_mask || a.write_mask[pool] != 0); };
+  auto issue = [&](int64_t pool, int s) {
+    uint8_t* dst = mybuf + s * 2 * L::kPoolBytes;
+    mbar_arrive_expect_tx(&bars[s], 2 * L::kPoolBytes);
+    bulk_load(dst, a.slot_k + pool * P * kD, L::kPoolBytes, &bars[s]);
+    bulk_load(dst + L::kPoolBytes, a.slot_score + pool * P * kD, L::kPoolBytes, &bars[s]);
+  };
+  uint32_t parity = 0, armed = 0;  // per-stage bits
+  if (lane == 0) {
+    for (int s = 0; s < kBulkStages; ++s) {
+      const int64_t pool = first + s * W;
+      if (wanted(pool)) issue(pool, s);
+    }
+  }
+  for (int s = 0; s < kBulkStages; ++s)
+    if (wanted(first + s * W)) armed |= 1u << s;
+
+  int s = 0;
+  for (int64_t pool = first; pool < a.n_pools; pool += W) {
+    if (armed & (1u << s)) {
+      if (!mbar_wait(&bars[s], (parity >> s) & 1u)) {
+        if (lane == 0) flag_error(a.err, CKV_DEVERR_TIMEOUT);
+        for (int x = 0; x < kBulkStages; ++x)
+          if (x != s && (armed & (1u << x))) (void)mbar_wait(&bars[x], (parity >> x) & 1u);
+        return;
+      }
+      parity ^= 1u << s;
+      armed &= ~(1u << s);
+      const uint8_t* kb = mybuf + s * 2 * L::kPoolBytes;
+      const uint8_t* sb = kb + L::kPoolBytes;
+      uint2 kr[P], sr[P];
+#pragma unroll
+      for (int j = 0; j < P; ++j) {
+        kr[j] = reinterpret_cast<const uint2*>(kb + j * kD * 2)[lane];
+        sr[j] = reinterpret_cast<const uint2*>(sb + j * kD * 2)[lane];
+      }
+      __syncwarp();
+      // the stage is free again: prefetch the pool kBulkStages turns ahead
+      const int64_t ahead = pool + kBulkStages * W;
+      if (wanted(ahead)) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          issue(ahead, s);
+        }
+        armed |= 1u << s;
+      }
+      float x[4], xb[4], yb[4], scale;
+      uint32_t codes;
+      pool_softmax<P>(kr, sr, s_ape, lane, x);
+      rotate_quantize<kRound>(x, lane, codes, scale, xb, yb);
+      if (a.write_cache) {
+        const int64_t loc = a.loc[pool];
+        if (loc < 0 || loc >= a.num_pages * a.page_size) {
+          if (lane == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
+        } else {
+          cache_write(a.cache, a.page_size, loc, lane, codes, scale);
+        }
+      }
+      if (a.out_fp8) {
+        reinterpret_cast<uint32_t*>(a.out_fp8 + pool * kD)[lane] = codes;
+        if (lane == 0) a.out_scale[pool] = scale;
+      }
+      write_taps(a.tap_x, a.tap_xb, a.tap_yb, pool, lane, x, xb, yb);
+    } else {
+      const int64_t ahead = pool + kBulkStages * W;
+      if (wanted(ahead)) {
+        if (lane == 0) issue(ahead, s);
+        armed |= 1u << s;
+      }
+    }
+    if (++s == kBulkStages) s = 0;
+  }
+}
+
 // Decode / verify update: warp w of CTA c handles request c*8 + w and walks its
 // N tokens in order.  A closing token reads ring slots 0..P-2 with ordinary
 // (coherent) loads: the same lane stashed any of them earlier in this call,
@@ -272,8 +387,26 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   reinterpret_cast<uint2*>(base + P * kD)[lane] = ld_stream_u2(a.score + i * kD + 4 * lane);
 }
 
+constexpr int64_t kBulkMinPools = 4096;
+
+template <int P, bool kRound>
+cudaError_t compress_bulk(const KpoolCompressArgs& a, cudaStream_t s) {
+  auto kern = kpool_compress_bulk_kernel<P, kRound>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       BulkLayout<P>::kBytes);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  kern<<<sms, kBulkWarps * 32, BulkLayout<P>::kBytes, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <int P>
 cudaError_t compress_p(const KpoolCompressArgs& a, bool round_scale, cudaStream_t s) {
+  const int v = kpool_compress_variant();
+  if (v == 2 || (v == 0 && a.n_pools >= kBulkMinPools))
+    return round_scale ? compress_bulk<P, true>(a, s) : compress_bulk<P, false>(a, s);
   const dim3 grid(static_cast<unsigned>((a.n_pools + kWarpsPerCta - 1) / kWarpsPerCta));
   if (round_scale)
     kpool_compress_kernel<P, true><<<grid, kWarpsPerCta * 32, 0, s>>>(a);

@@ -240,6 +240,16 @@ ckv_status ckv_c128_online_prefill(float* state, int64_t num_slots, const void* 
 int32_t ckv_c128_prefill_set_variant(int32_t variant);
 
 /*
+ * Kernel choice for ckv_kpool_compress (process-wide).
+ *   0 = automatic (default): the persistent bulk-copy pipeline for at least
+ *       4096 pools, otherwise one warp per pool;
+ *   1 = always one warp per pool;  2 = always the bulk-copy pipeline.
+ * Both compute the same function.  Returns the previous setting, or -1 (and
+ * changes nothing) for an unknown value.
+ */
+int32_t ckv_kpool_compress_set_variant(int32_t variant);
+
+/*
  * Host planner for the online c128 prefill (sglang c128_online.cuh page,
  * plan_online_prefill_host).  Request i covers global positions
  * [seq_lens[i] - extend_lens[i], seq_lens[i]) and ragged rows that follow the

@@ -30,6 +30,14 @@ def ck():
     return ck
 
 
+@pytest.fixture(params=[1, 2], ids=["warp_per_pool", "bulk_pipeline"])
+def cvariant(request, ck):
+    """Run a one-shot compression test with each kernel."""
+    prev = ck.ckv_kpool_compress_set_variant(request.param)
+    yield request.param
+    ck.ckv_kpool_compress_set_variant(prev)
+
+
 def _to(d, dev):
     return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
 
@@ -62,7 +70,7 @@ def check_rows(ora, gpu_x, gpu_xb, gpu_yb, gpu_q, gpu_s, ref, round_scale, what)
 # ------------------------------------------------------------------ one-shot
 @pytest.mark.parametrize("P", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("round_scale", [True, False])
-def test_kpool_compress_vs_oracle(ck, ora, P, round_scale):
+def test_kpool_compress_vs_oracle(cvariant, ck, ora, P, round_scale):
     from compressed_kv_attention_gated_gb300 import synth
 
     n = 203  # several CTAs of 8 pools and a ragged tail
@@ -108,7 +116,7 @@ def test_kpool_compress_vs_oracle(ck, ora, P, round_scale):
     assert np.all(gcache.reshape(-1)[mask] == 0x5A), "bytes outside the written rows changed"
 
 
-def test_kpool_compress_write_mask_and_cache_only(ck, ora):
+def test_kpool_compress_write_mask_and_cache_only(cvariant, ck, ora):
     n, P = 77, 16
     g = torch.Generator().manual_seed(7)
     slot_k = torch.randn((n, P, D), generator=g).to(torch.bfloat16)
@@ -136,7 +144,7 @@ def test_kpool_compress_write_mask_and_cache_only(ck, ora):
     assert_fp8_within_one(gq[w][same_s], rq[w][same_s], "masked compress")
 
 
-def test_kpool_compress_bad_loc_flags_and_skips(ck):
+def test_kpool_compress_bad_loc_flags_and_skips(cvariant, ck):
     n, P = 16, 16
     slot = torch.randn((n, P, D), device="cuda").to(torch.bfloat16)
     ape = torch.zeros((P, D), device="cuda")
@@ -152,6 +160,44 @@ def test_kpool_compress_bad_loc_flags_and_skips(ck):
     c = u8(cache).reshape(-1)
     assert np.all(c[3 * D:4 * D] == 7) and np.all(c[5 * D:6 * D] == 7)
     assert not np.all(c[4 * D:5 * D] == 7)
+
+
+@pytest.mark.parametrize("n,masked", [(9001, False), (12007, True)])
+def test_kpool_compress_many_pools_per_warp(cvariant, ck, ora, n, masked):
+    """More pools than warps in the persistent grid, so every warp reuses its
+    stages several times (and skips masked pools)."""
+    P = 16
+    g = torch.Generator().manual_seed(n)
+    slot_k = torch.randn((n, P, D), generator=g).to(torch.bfloat16)
+    slot_s = (torch.randn((n, P, D), generator=g) * 2).to(torch.bfloat16)
+    ape = torch.randn((P, D), generator=g) * 0.1
+    ps = 64
+    pages = (n + ps - 1) // ps
+    loc = torch.randperm(pages * ps, generator=g)[:n].to(torch.int64)
+    wm = (torch.rand((n,), generator=g) < 0.7) if masked else None
+    cache0 = torch.full((pages, ps, D + 4), 0x11, dtype=torch.uint8)
+    cache = cache0.cuda()
+    kw = {}
+    if not masked:
+        kw["out_fp8"] = torch.zeros((n, D), dtype=torch.uint8, device="cuda")
+        kw["out_scale"] = torch.zeros((n,), dtype=torch.float32, device="cuda")
+    err = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    ck.ckv_kpool_compress(slot_k.cuda(), slot_s.cuda(), ape.cuda(), kv_cache=cache, loc=loc.cuda(),
+                          write_mask=None if wm is None else wm.cuda(), err_word=err, **kw)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref_cache = u8(cache0).copy()
+    ora.kpool_compress(ref_cache, ps, bf16_bits(slot_k), bf16_bits(slot_s), f32(ape), loc.numpy(),
+                       write_mask=None if wm is None else wm.numpy().astype(np.uint8))
+    gq, gs = cache_rows(u8(cache), ps, D, loc.numpy())
+    rq, rs = cache_rows(ref_cache, ps, D, loc.numpy())
+    w = np.ones(n, bool) if wm is None else wm.numpy()
+    assert np.all(gq[~w] == 0x11)
+    same = gs[w] == rs[w]
+    assert same.mean() > 0.97
+    assert_fp8_within_one(gq[w][same], rq[w][same], "many pools")
+    if not masked:
+        np.testing.assert_array_equal(u8(kw["out_fp8"]), gq)
 
 
 # -------------------------------------------------------------- decode update
