@@ -33,19 +33,21 @@ constexpr int kD = 128;          // pooled head dim (the rotation is 128-point)
 constexpr int kRowBytes = kD + 4; // FP8 row + fp32 scale per cache row
 
 // Softmax-weighted pool of P slots for the lane's 4 channels.
-// kr/sr: slot rows of keys/scores, 4 bf16 each; s_ape: [P][128] fp32 in smem.
+// kr/sr: slot rows of keys/scores, 4 bf16 each; s_ape2: [P][128] fp32 in smem,
+// the bias already multiplied by log2(e), so each logit in the log2 domain is
+// one FMA (score * log2(e) + bias') and each weight one ex2 of a difference.
 template <int P>
 __device__ __forceinline__ void pool_softmax(const uint2 (&kr)[P], const uint2 (&sr)[P],
-                                             const float* s_ape, int lane, float (&x)[4]) {
+                                             const float* s_ape2, int lane, float (&x)[4]) {
   float z[P][4];
   float m[4] = {kNegBig, kNegBig, kNegBig, kNegBig};
 #pragma unroll
   for (int j = 0; j < P; ++j) {
-    const float4 a = reinterpret_cast<const float4*>(s_ape + j * kD)[lane];
-    z[j][0] = bf16_lo(sr[j].x) + a.x;
-    z[j][1] = bf16_hi(sr[j].x) + a.y;
-    z[j][2] = bf16_lo(sr[j].y) + a.z;
-    z[j][3] = bf16_hi(sr[j].y) + a.w;
+    const float4 a = reinterpret_cast<const float4*>(s_ape2 + j * kD)[lane];
+    z[j][0] = fmaf(bf16_lo(sr[j].x), kLog2e, a.x);
+    z[j][1] = fmaf(bf16_hi(sr[j].x), kLog2e, a.y);
+    z[j][2] = fmaf(bf16_lo(sr[j].y), kLog2e, a.z);
+    z[j][3] = fmaf(bf16_hi(sr[j].y), kLog2e, a.w);
 #pragma unroll
     for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], z[j][i]);
   }
@@ -56,11 +58,11 @@ __device__ __forceinline__ void pool_softmax(const uint2 (&kr)[P], const uint2 (
     for (int j = 0; j < P; ++j) {
       const uint32_t w = (i < 2) ? kr[j].x : kr[j].y;
       const float k = (i & 1) ? bf16_hi(w) : bf16_lo(w);
-      const float e = exp_diff(z[j][i], m[i]);
+      const float e = fast_exp2(z[j][i] - m[i]);
       den += e;
       acc = fmaf(e, k, acc);
     }
-    x[i] = acc / den;
+    x[i] = __fdividef(acc, den);  // den in [1, P]
   }
 }
 
@@ -93,11 +95,13 @@ __device__ __forceinline__ void rotate_quantize(const float (&x)[4], int lane, u
   }
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1) {  // spans 4, 8, 16, 32, 64: partner lane l ^ m
-    const bool upper = (lane & m) != 0;
+    // lower lane: a + o; upper lane: o - a.  fma(a, -1, o) rounds o - a once,
+    // exactly like a subtraction, so one FMA serves both halves.
+    const float sgn = (lane & m) ? -1.f : 1.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float o = __shfl_xor_sync(0xFFFFFFFFu, a[i], m);
-      a[i] = upper ? (o - a[i]) : (a[i] + o);
+      a[i] = fmaf(a[i], sgn, o);
     }
   }
   const float c = __uint_as_float(0x3DB504F3u);  // fp32(1/sqrt(128))
@@ -111,16 +115,22 @@ __device__ __forceinline__ void rotate_quantize(const float (&x)[4], int lane, u
   for (int m = 16; m >= 1; m >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, m));
   am = fmaxf(am, 1e-4f);
   const float v = am * __uint_as_float(0x3B124925u);  // absmax * fp32(1/448)
+  float q[4];
   if (kRound) {
-    // smallest power of two >= v (v is a positive normal number)
+    // smallest power of two >= v (v is a positive normal number); dividing by a
+    // power of two is exact, so multiplying by its (exact) reciprocal is the same
+    // IEEE quotient
     const uint32_t bits = __float_as_uint(v);
-    scale = (bits & 0x007FFFFFu) ? __uint_as_float((bits & 0x7F800000u) + 0x00800000u) : v;
+    const uint32_t e = (bits & 0x007FFFFFu) ? (bits & 0x7F800000u) + 0x00800000u : (bits & 0x7F800000u);
+    scale = __uint_as_float(e);
+    const float inv = __uint_as_float((254u << 23) - e);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = fminf(fmaxf(yb[i] * inv, -448.f), 448.f);
   } else {
     scale = v;
-  }
-  float q[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) q[i] = fminf(fmaxf(__fdiv_rn(yb[i], scale), -448.f), 448.f);
+    for (int i = 0; i < 4; ++i) q[i] = fminf(fmaxf(__fdiv_rn(yb[i], scale), -448.f), 448.f);
+  }
   const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(q[0], q[1]), __NV_SATFINITE, __NV_E4M3);
   const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(q[2], q[3]), __NV_SATFINITE, __NV_E4M3);
   codes = (lo & 0xFFFFu) | (hi << 16);
@@ -146,10 +156,17 @@ __device__ __forceinline__ void cache_write(uint8_t* cache, int64_t page_size, i
   if (lane == 0) *reinterpret_cast<float*>(base + page_size * kD + 4 * tok) = scale;
 }
 
+// Stage the [P][128] bias table in shared memory, multiplied by log2(e).
 template <int P>
-__device__ __forceinline__ void stage_ape(float* s_ape, const float* ape) {
-  for (int i = threadIdx.x; i < P * kD / 4; i += blockDim.x)
-    reinterpret_cast<float4*>(s_ape)[i] = ld_shared_ro_f4(ape + 4 * i);
+__device__ __forceinline__ void stage_ape(float* s_ape2, const float* ape) {
+  for (int i = threadIdx.x; i < P * kD / 4; i += blockDim.x) {
+    float4 v = ld_shared_ro_f4(ape + 4 * i);
+    v.x *= kLog2e;
+    v.y *= kLog2e;
+    v.z *= kLog2e;
+    v.w *= kLog2e;
+    reinterpret_cast<float4*>(s_ape2)[i] = v;
+  }
   __syncthreads();
 }
 
@@ -305,9 +322,13 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 1)
 }
 
 // Decode / verify update: warp w of CTA c handles request c*8 + w and walks its
-// N tokens in order.  A closing token reads ring slots 0..P-2 with ordinary
-// (coherent) loads: the same lane stashed any of them earlier in this call,
-// so program order makes those stores visible.
+// N tokens in order.  The index triples and key/score rows of kPrefetch tokens
+// are loaded together before they are processed one by one, so the only
+// dependent global round trip per group is a closing pool's ring read.  That
+// read uses ordinary (coherent) loads: the same lane stashed any of those slots
+// earlier in this call, so program order makes its stores visible.
+constexpr int kPrefetch = 4;
+
 template <int P, bool kRound>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
     kpool_decode_kernel(const __grid_constant__ KpoolDecodeArgs a) {
@@ -318,50 +339,62 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   if (b >= a.B) return;
   const int64_t cache_rows = a.num_pages * a.page_size;
 
-  for (int t = 0; t < a.N; ++t) {
-    const int64_t idx = static_cast<int64_t>(b) * a.N + t;
-    const int32_t loc = a.slot_mapping[idx];
-    const int32_t pos = a.positions[idx];
-    const int32_t tslot = a.tail_slot_mapping[idx];
-    const uint2 kc = ld_stream_u2(a.key + b * a.key_sb + t * a.key_st + 4 * lane);
-    const uint2 sc = ld_stream_u2(a.score + b * a.score_sb + t * a.score_st + 4 * lane);
-
-    const int slot = max(pos, 0) & (P - 1);
-    const bool pos_valid = loc >= 0 && pos >= 0;
-    const bool stash_valid = pos >= 0 && tslot >= 0;
-    const bool closes = pos_valid && slot == P - 1;
-    if (!closes && !stash_valid) continue;
-    const int64_t block = static_cast<int64_t>(max(tslot, 0)) / P;
-    if (block >= a.num_blocks) {
-      if (lane == 0) flag_error(a.err, CKV_DEVERR_TAIL_BLOCK);
-      continue;
-    }
-    uint16_t* kring = a.ring + block * 2 * P * kD;
-    uint16_t* sring = kring + P * kD;
-
-    if (closes) {
-      if (loc >= cache_rows) {
-        if (lane == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
-      } else {
-        uint2 kr[P], sr[P];
+  for (int t0 = 0; t0 < a.N; t0 += kPrefetch) {
+    int32_t loc[kPrefetch], pos[kPrefetch], tslot[kPrefetch];
+    uint2 kc[kPrefetch], sc[kPrefetch];
 #pragma unroll
-        for (int j = 0; j < P - 1; ++j) {
-          kr[j] = *reinterpret_cast<const uint2*>(kring + j * kD + 4 * lane);
-          sr[j] = *reinterpret_cast<const uint2*>(sring + j * kD + 4 * lane);
-        }
-        kr[P - 1] = kc;
-        sr[P - 1] = sc;
-        float x[4], xb[4], yb[4], scale;
-        uint32_t codes;
-        pool_softmax<P>(kr, sr, s_ape, lane, x);
-        rotate_quantize<kRound>(x, lane, codes, scale, xb, yb);
-        cache_write(a.cache, a.page_size, loc, lane, codes, scale);
-        write_taps(a.tap_x, a.tap_xb, a.tap_yb, idx, lane, x, xb, yb);
+    for (int i = 0; i < kPrefetch; ++i) {
+      const int t = t0 + i;
+      if (t < a.N) {
+        const int64_t idx = static_cast<int64_t>(b) * a.N + t;
+        loc[i] = a.slot_mapping[idx];
+        pos[i] = a.positions[idx];
+        tslot[i] = a.tail_slot_mapping[idx];
+        kc[i] = ld_stream_u2(a.key + b * a.key_sb + t * a.key_st + 4 * lane);
+        sc[i] = ld_stream_u2(a.score + b * a.score_sb + t * a.score_st + 4 * lane);
+      } else {
+        loc[i] = pos[i] = tslot[i] = -1;  // past N: neither closes nor stashes
+        kc[i] = sc[i] = make_uint2(0u, 0u);
       }
     }
-    if (stash_valid) {
-      *reinterpret_cast<uint2*>(kring + slot * kD + 4 * lane) = kc;
-      *reinterpret_cast<uint2*>(sring + slot * kD + 4 * lane) = sc;
+#pragma unroll
+    for (int i = 0; i < kPrefetch; ++i) {
+      const int slot = max(pos[i], 0) & (P - 1);
+      const bool pos_valid = loc[i] >= 0 && pos[i] >= 0;
+      const bool stash_valid = pos[i] >= 0 && tslot[i] >= 0;
+      const bool closes = pos_valid && slot == P - 1;
+      if (!closes && !stash_valid) continue;
+      const int64_t block = static_cast<int64_t>(max(tslot[i], 0)) / P;
+      if (block >= a.num_blocks) {
+        if (lane == 0) flag_error(a.err, CKV_DEVERR_TAIL_BLOCK);
+        continue;
+      }
+      uint16_t* kring = a.ring + block * 2 * P * kD;
+      uint16_t* sring = kring + P * kD;
+      if (closes) {
+        if (loc[i] >= cache_rows) {
+          if (lane == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
+        } else {
+          uint2 kr[P], sr[P];
+#pragma unroll
+          for (int j = 0; j < P - 1; ++j) {
+            kr[j] = *reinterpret_cast<const uint2*>(kring + j * kD + 4 * lane);
+            sr[j] = *reinterpret_cast<const uint2*>(sring + j * kD + 4 * lane);
+          }
+          kr[P - 1] = kc[i];
+          sr[P - 1] = sc[i];
+          float x[4], xb[4], yb[4], scale;
+          uint32_t codes;
+          pool_softmax<P>(kr, sr, s_ape, lane, x);
+          rotate_quantize<kRound>(x, lane, codes, scale, xb, yb);
+          cache_write(a.cache, a.page_size, loc[i], lane, codes, scale);
+          write_taps(a.tap_x, a.tap_xb, a.tap_yb, static_cast<int64_t>(b) * a.N + t0 + i, lane, x, xb, yb);
+        }
+      }
+      if (stash_valid) {
+        *reinterpret_cast<uint2*>(kring + slot * kD + 4 * lane) = kc[i];
+        *reinterpret_cast<uint2*>(sring + slot * kD + 4 * lane) = sc[i];
+      }
     }
   }
 }
