@@ -183,6 +183,8 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   if (pool >= a.n_pools) return;
   if (a.write_mask && a.write_mask[pool] == 0) return;
 
+  // the cache location travels with the rows, not after the arithmetic
+  const int64_t loc = a.write_cache ? a.loc[pool] : 0;
   uint2 kr[P], sr[P];
   const uint16_t* kb = a.slot_k + pool * P * kD + 4 * lane;
   const uint16_t* sb = a.slot_score + pool * P * kD + 4 * lane;
@@ -197,7 +199,6 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   rotate_quantize<kRound>(x, lane, codes, scale, xb, yb);
 
   if (a.write_cache) {
-    const int64_t loc = a.loc[pool];
     if (loc < 0 || loc >= a.num_pages * a.page_size) {
       if (lane == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
     } else {
@@ -264,8 +265,13 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 1)
   for (int s = 0; s < kBulkStages; ++s)
     if (wanted(first + s * W)) armed |= 1u << s;
 
+  // cache locations are fetched one pool ahead so that no global load sits
+  // between a pool's arithmetic and its store
+  int64_t loc_next = (a.write_cache && first < a.n_pools) ? a.loc[first] : 0;
   int s = 0;
   for (int64_t pool = first; pool < a.n_pools; pool += W) {
+    const int64_t loc = loc_next;
+    if (a.write_cache && pool + W < a.n_pools) loc_next = a.loc[pool + W];
     if (armed & (1u << s)) {
       if (!mbar_wait(&bars[s], (parity >> s) & 1u)) {
         if (lane == 0) flag_error(a.err, CKV_DEVERR_TIMEOUT);
@@ -298,7 +304,6 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 1)
       pool_softmax<P>(kr, sr, s_ape, lane, x);
       rotate_quantize<kRound>(x, lane, codes, scale, xb, yb);
       if (a.write_cache) {
-        const int64_t loc = a.loc[pool];
         if (loc < 0 || loc >= a.num_pages * a.page_size) {
           if (lane == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
         } else {
