@@ -178,26 +178,29 @@ class Step:
         self._accounting()
 
     # -- calls -------------------------------------------------------------
-    def call(self, i):
+    def call(self, i, pdl=False):
+        """Call i of the step; with pdl every launch is a programmatic dependent
+        launch on its predecessor (each kernel still waits for it on the device
+        before touching memory, but its launch overlaps the predecessor's tail)."""
         ck, pd, cd, cp, lc = self.ck, self.pd, self.cd, self.cp, self.lc
         if i == 0:
             ck.ckv_kpool_decode_update(pd["kv_cache"], pd["ring"], pd["tail_slot_mapping"], pd["slot_mapping"],
                                        pd["positions"], pd["key"], pd["score"], pd["ape"], round_scale=True,
-                                       err_word=self.err)
+                                       use_pdl=pdl, err_word=self.err)
         elif i == 1:
             ck.ckv_c128_online_decode(cd["state"], cd["input"], cd["out"], cd["ape"], cd["indices"], cd["seq_lens"],
-                                      err_word=self.err)
+                                      use_pdl=pdl, err_word=self.err)
         elif i == 2:
             c, nc, w, nw = self.plans["cp"][:4]
             ck.ckv_c128_online_prefill(cp["state"], cp["input"], cp["out"], cp["ape"], cp["indices"], c, nc, w, nw,
-                                       err_word=self.err)
+                                       use_pdl=pdl, err_word=self.err)
         elif i == 3:
             c, nc, w, nw = self.plans["lc"][:4]
             ck.ckv_c128_online_prefill(lc["state"], lc["input"], lc["out"], lc["ape"], lc["indices"], c, nc, w, nw,
-                                       err_word=self.err)
+                                       use_pdl=pdl, err_word=self.err)
         elif i == 4:
             ck.ckv_kpool_compress(lc["slot_k"], lc["slot_score"], lc["ape_pool"], kv_cache=lc["kv_cache"],
-                                  loc=lc["loc"], round_scale=True, err_word=self.err)
+                                  loc=lc["loc"], round_scale=True, use_pdl=pdl, err_word=self.err)
 
     def launches(self):
         n = 0
@@ -556,6 +559,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pdl", action="store_true", help="plain stream order between the five calls")
     ap.add_argument("--prefill-variant", type=int, default=0,
                     help="compress-pass kernel: 0 auto, 1 one CTA per segment, 2 TMA pipeline")
     ap.add_argument("--kpool-variant", type=int, default=0,
@@ -589,25 +593,40 @@ def main():
     nk = len(step.names)
     stream = torch.cuda.Stream(dev)
     torch.cuda.synchronize()
+    pdl = not args.no_pdl
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             for i in range(nk):
-                step.call(i)
+                step.call(i, pdl)
         stream.synchronize()
         assert int(step.err.item()) == 0, f"kernel error word {int(step.err.item()):#x}"
         K = args.steps
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(K)]
+        # timed region: K whole steps, launches chained by programmatic dependent launch
+        e_start = torch.cuda.Event(enable_timing=True)
+        e_end = torch.cuda.Event(enable_timing=True)
         _barrier(ws)
         torch.cuda.synchronize()
         with ClockSampler(local) as clk:
+            e_start.record(stream)
             for k in range(K):
-                evs[k][0].record(stream)
                 for i in range(nk):
-                    step.call(i)
-                    evs[k][i + 1].record(stream)
+                    step.call(i, pdl)
+            e_end.record(stream)
             stream.synchronize()
         _barrier(ws)
-    elapsed_ms = evs[0][0].elapsed_time(evs[-1][nk])
+        elapsed_ms = e_start.elapsed_time(e_end)
+        # breakdown: the same steps with an event between consecutive calls (an event
+        # between two launches removes the programmatic overlap, so this loop is
+        # timed on its own and used only to attribute time to the five calls)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(K)]
+        torch.cuda.synchronize()
+        for k in range(K):
+            evs[k][0].record(stream)
+            for i in range(nk):
+                step.call(i, False)
+                evs[k][i + 1].record(stream)
+        stream.synchronize()
+        breakdown_ms = evs[0][0].elapsed_time(evs[-1][nk]) / K
     per_kernel_ms = [statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)) for i in range(nk)]
     elapsed_ms = _max_over_ranks(elapsed_ms, ws, dev)
     ms_per_step = elapsed_ms / K
@@ -668,7 +687,8 @@ def main():
             "config": {"workload": WORKLOAD, "tokens_per_step": int(tokens_step), "parallelism": f"replicas x{ws}",
                        "l2": "inputs larger than L2 (step working set ~3.7 GB >> 126 MB L2)"},
             "step_hbm_gbs": round(step_gbs, 1), "step_frac_of_peak": round(step_gbs / peak, 4),
-            "kernels": kernels, "roofline": roofline, "clocks": clk.summary(),
+            "launch_chaining": "programmatic dependent launch" if pdl else "stream order",
+            "breakdown_ms_per_step": round(breakdown_ms, 4), "kernels": kernels, "roofline": roofline, "clocks": clk.summary(),
             "gpu_launches": step.launches() * K, "e2e": e2e, "cpu_baseline": cpu,
         }), flush=True)
     if ws > 1:

@@ -67,12 +67,14 @@ def load():
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                 ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                 ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                ctypes.c_void_p]
             L.ckv_kpool_compress.argtypes = [
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                ctypes.c_void_p]
             L.ckv_kpool_seed_tail.argtypes = [
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                 ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
@@ -140,7 +142,7 @@ def _need(cond, msg):
 # ------------------------------------------------------------ pooled path
 def ckv_kpool_decode_update(kv_cache, tail_ring, tail_slot_mapping, slot_mapping, positions, key,
                             score, ape, round_scale=True, tap_x=None, tap_xb=None, tap_yb=None,
-                            err_word=None, stream=None):
+                            use_pdl=False, err_word=None, stream=None):
     """Pooled decode/verify update; see ckv_kpool_decode_update in include/ckv.h.
 
     kv_cache uint8 [pages, page_size, D+4]; tail_ring bf16 [blocks, 2, P, D];
@@ -167,13 +169,13 @@ def ckv_kpool_decode_update(kv_cache, tail_ring, tail_slot_mapping, slot_mapping
         _ptr(kv_cache), kv_cache.shape[0], kv_cache.shape[1], _ptr(tail_ring), tail_ring.shape[0],
         _ptr(tail_slot_mapping), _ptr(slot_mapping), _ptr(positions), _ptr(key), key.stride(0),
         key.stride(1), _ptr(score), score.stride(0), score.stride(1), _ptr(ape), B, N, P, D,
-        int(bool(round_scale)), _ptr(tap_x), _ptr(tap_xb), _ptr(tap_yb), _ptr(err_word),
+        int(bool(round_scale)), _ptr(tap_x), _ptr(tap_xb), _ptr(tap_yb), int(bool(use_pdl)), _ptr(err_word),
         _stream(stream, key)))
 
 
 def ckv_kpool_compress(slot_k, slot_score, ape, kv_cache=None, loc=None, write_mask=None,
                        write_cache=True, out_fp8=None, out_scale=None, round_scale=True, tap_x=None,
-                       tap_xb=None, tap_yb=None, err_word=None, stream=None):
+                       tap_xb=None, tap_yb=None, use_pdl=False, err_word=None, stream=None):
     """One-shot pooled compression; see ckv_kpool_compress in include/ckv.h.
 
     slot_k/slot_score bf16 [n, P, D] contiguous; ape float32 [P, D]; loc int64 [n];
@@ -207,7 +209,7 @@ def ckv_kpool_compress(slot_k, slot_score, ape, kv_cache=None, loc=None, write_m
         _ptr(kv_cache) if write_cache else None, pages, ps, _ptr(slot_k), _ptr(slot_score), _ptr(ape),
         _ptr(loc) if write_cache else None, _ptr(write_mask), int(bool(write_cache)), _ptr(out_fp8),
         _ptr(out_scale), n, P, D, int(bool(round_scale)), _ptr(tap_x), _ptr(tap_xb), _ptr(tap_yb),
-        _ptr(err_word), _stream(stream, slot_k)))
+        int(bool(use_pdl)), _ptr(err_word), _stream(stream, slot_k)))
 
 
 def ckv_kpool_seed_tail(tail_ring, key, score, tslot, err_word=None, stream=None):

@@ -22,6 +22,7 @@
 
 #include "ckv_device.cuh"
 #include "ckv_launch.h"
+#include "ckv_launch_util.cuh"
 
 namespace ckv {
 namespace {
@@ -249,26 +250,10 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
   }
 }
 
-template <typename Args>
-cudaError_t launch(void (*k)(Args), dim3 grid, dim3 block, bool use_pdl, cudaStream_t s,
-                   const Args& args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = use_pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k, args);
-}
-
 template <int D, typename InT>
 cudaError_t decode_d(const C128DecodeArgs& a, bool use_pdl, cudaStream_t s) {
   const dim3 grid((a.B + kDecodeWarps - 1) / kDecodeWarps);
-  return launch(c128_decode_kernel<D, InT>, grid, dim3(kDecodeWarps * 32), use_pdl, s, a);
+  return launch_ex(c128_decode_kernel<D, InT>, grid, dim3(kDecodeWarps * 32), 0, use_pdl, s, a);
 }
 
 constexpr uint32_t kTmaMinSegments = 32;
@@ -290,14 +275,14 @@ cudaError_t prefill_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
     }
     if (e == cudaErrorNotSupported) {
       const dim3 grid(static_cast<unsigned>(a.num_compress) * S);
-      e = launch(c128_prefill_kernel<D, InT, false>, grid, dim3(kPrefillWarps * 32), use_pdl, s, a);
+      e = launch_ex(c128_prefill_kernel<D, InT, false>, grid, dim3(kPrefillWarps * 32), 0, use_pdl, s, a);
     }
     if (e != cudaSuccess) return e;
   }
   if (a.num_write) {
     const dim3 grid(static_cast<unsigned>(a.num_write) * S);
-    cudaError_t e = launch(c128_prefill_kernel<D, InT, true>, grid, dim3(kPrefillWarps * 32),
-                           use_pdl, s, a);
+    cudaError_t e =
+        launch_ex(c128_prefill_kernel<D, InT, true>, grid, dim3(kPrefillWarps * 32), 0, use_pdl, s, a);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

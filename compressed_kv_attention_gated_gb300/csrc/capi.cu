@@ -69,8 +69,8 @@ ckv_status ckv_kpool_decode_update(uint8_t* kv_cache, int64_t num_pages, int32_t
                                    const uint16_t* score, int64_t score_stride_b,
                                    int64_t score_stride_t, const float* ape, int32_t B, int32_t N,
                                    int32_t P, int32_t D, int32_t round_scale, float* tap_x,
-                                   uint16_t* tap_xb, uint16_t* tap_yb, int32_t* err_word,
-                                   void* stream) {
+                                   uint16_t* tap_xb, uint16_t* tap_yb, int32_t use_pdl,
+                                   int32_t* err_word, void* stream) {
   if (B < 0 || N < 0 || D != 128 || !pool_size_ok(P) || page_size <= 0 || num_pages < 0 ||
       num_tail_blocks < 0)
     return CKV_ERR_SHAPE;
@@ -107,7 +107,7 @@ ckv_status ckv_kpool_decode_update(uint8_t* kv_cache, int64_t num_pages, int32_t
   a.err = err_word;
   a.B = B;
   a.N = N;
-  return cuda_status(ckv::launch_kpool_decode_update(a, P, round_scale != 0,
+  return cuda_status(ckv::launch_kpool_decode_update(a, P, round_scale != 0, use_pdl != 0,
                                                      static_cast<cudaStream_t>(stream)));
 }
 
@@ -116,7 +116,7 @@ ckv_status ckv_kpool_compress(uint8_t* kv_cache, int64_t num_pages, int32_t page
                               const int64_t* loc, const uint8_t* write_mask, int32_t write_cache,
                               uint8_t* out_fp8, float* out_scale, int64_t n_pools, int32_t P,
                               int32_t D, int32_t round_scale, float* tap_x, uint16_t* tap_xb,
-                              uint16_t* tap_yb, int32_t* err_word, void* stream) {
+                              uint16_t* tap_yb, int32_t use_pdl, int32_t* err_word, void* stream) {
   if (n_pools < 0 || D != 128 || !pool_size_ok(P)) return CKV_ERR_SHAPE;
   if (!write_cache && !out_fp8) return CKV_ERR_SHAPE;        // nothing requested
   if ((out_fp8 == nullptr) != (out_scale == nullptr)) return CKV_ERR_NULL;
@@ -146,8 +146,8 @@ ckv_status ckv_kpool_compress(uint8_t* kv_cache, int64_t num_pages, int32_t page
   a.err = err_word;
   a.n_pools = n_pools;
   a.write_cache = write_cache != 0;
-  return cuda_status(
-      ckv::launch_kpool_compress(a, P, round_scale != 0, static_cast<cudaStream_t>(stream)));
+  return cuda_status(ckv::launch_kpool_compress(a, P, round_scale != 0, use_pdl != 0,
+                                                static_cast<cudaStream_t>(stream)));
 }
 
 ckv_status ckv_kpool_seed_tail(uint16_t* tail_ring, int64_t num_tail_blocks, const uint16_t* key,

@@ -91,9 +91,9 @@ struct C128PrefillArgs {
 };
 
 cudaError_t launch_kpool_compress(const KpoolCompressArgs& a, int P, bool round_scale,
-                                  cudaStream_t s);
+                                  bool use_pdl, cudaStream_t s);
 cudaError_t launch_kpool_decode_update(const KpoolDecodeArgs& a, int P, bool round_scale,
-                                       cudaStream_t s);
+                                       bool use_pdl, cudaStream_t s);
 cudaError_t launch_kpool_seed_tail(const KpoolSeedArgs& a, int P, cudaStream_t s);
 cudaError_t launch_c128_decode(const C128DecodeArgs& a, int D, int in_dtype, bool use_pdl,
                                cudaStream_t s);

@@ -24,6 +24,7 @@
 // The pooled path is memory bound (no dense contraction); no tensor cores.
 #include "ckv_device.cuh"
 #include "ckv_launch.h"
+#include "ckv_launch_util.cuh"
 #include "ckv_tma.cuh"
 
 namespace ckv {
@@ -156,9 +157,12 @@ __device__ __forceinline__ void cache_write(uint8_t* cache, int64_t page_size, i
   if (lane == 0) *reinterpret_cast<float*>(base + page_size * kD + 4 * tok) = scale;
 }
 
-// Stage the [P][128] bias table in shared memory, multiplied by log2(e).
+// Wait for the preceding grid (programmatic dependent launch; a no-op
+// otherwise), then stage the [P][128] bias table in shared memory, multiplied
+// by log2(e), and let the next grid in the stream begin launching.
 template <int P>
 __device__ __forceinline__ void stage_ape(float* s_ape2, const float* ape) {
+  pdl_wait();
   for (int i = threadIdx.x; i < P * kD / 4; i += blockDim.x) {
     float4 v = ld_shared_ro_f4(ape + 4 * i);
     v.x *= kLog2e;
@@ -168,6 +172,7 @@ __device__ __forceinline__ void stage_ape(float* s_ape2, const float* ape) {
     reinterpret_cast<float4*>(s_ape2)[i] = v;
   }
   __syncthreads();
+  pdl_trigger();
 }
 
 constexpr int kWarpsPerCta = 8;
@@ -428,7 +433,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
 constexpr int64_t kBulkMinPools = 4096;
 
 template <int P, bool kRound>
-cudaError_t compress_bulk(const KpoolCompressArgs& a, cudaStream_t s) {
+cudaError_t compress_bulk(const KpoolCompressArgs& a, bool use_pdl, cudaStream_t s) {
   auto kern = kpool_compress_bulk_kernel<P, kRound>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        BulkLayout<P>::kBytes);
@@ -436,31 +441,26 @@ cudaError_t compress_bulk(const KpoolCompressArgs& a, cudaStream_t s) {
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  kern<<<sms, kBulkWarps * 32, BulkLayout<P>::kBytes, s>>>(a);
-  return cudaGetLastError();
+  return launch_ex(kern, dim3(sms), dim3(kBulkWarps * 32), BulkLayout<P>::kBytes, use_pdl, s, a);
 }
 
 template <int P>
-cudaError_t compress_p(const KpoolCompressArgs& a, bool round_scale, cudaStream_t s) {
+cudaError_t compress_p(const KpoolCompressArgs& a, bool round_scale, bool use_pdl, cudaStream_t s) {
   const int v = kpool_compress_variant();
   if (v == 2 || (v == 0 && a.n_pools >= kBulkMinPools))
-    return round_scale ? compress_bulk<P, true>(a, s) : compress_bulk<P, false>(a, s);
+    return round_scale ? compress_bulk<P, true>(a, use_pdl, s) : compress_bulk<P, false>(a, use_pdl, s);
   const dim3 grid(static_cast<unsigned>((a.n_pools + kWarpsPerCta - 1) / kWarpsPerCta));
-  if (round_scale)
-    kpool_compress_kernel<P, true><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
-  else
-    kpool_compress_kernel<P, false><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  return round_scale
+             ? launch_ex(kpool_compress_kernel<P, true>, grid, dim3(kWarpsPerCta * 32), 0, use_pdl, s, a)
+             : launch_ex(kpool_compress_kernel<P, false>, grid, dim3(kWarpsPerCta * 32), 0, use_pdl, s, a);
 }
 
 template <int P>
-cudaError_t decode_p(const KpoolDecodeArgs& a, bool round_scale, cudaStream_t s) {
+cudaError_t decode_p(const KpoolDecodeArgs& a, bool round_scale, bool use_pdl, cudaStream_t s) {
   const dim3 grid((a.B + kWarpsPerCta - 1) / kWarpsPerCta);
-  if (round_scale)
-    kpool_decode_kernel<P, true><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
-  else
-    kpool_decode_kernel<P, false><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  return round_scale
+             ? launch_ex(kpool_decode_kernel<P, true>, grid, dim3(kWarpsPerCta * 32), 0, use_pdl, s, a)
+             : launch_ex(kpool_decode_kernel<P, false>, grid, dim3(kWarpsPerCta * 32), 0, use_pdl, s, a);
 }
 
 template <int P>
@@ -473,25 +473,25 @@ cudaError_t seed_p(const KpoolSeedArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_kpool_compress(const KpoolCompressArgs& a, int P, bool round_scale,
-                                  cudaStream_t s) {
+                                  bool use_pdl, cudaStream_t s) {
   switch (P) {
-    case 1: return compress_p<1>(a, round_scale, s);
-    case 2: return compress_p<2>(a, round_scale, s);
-    case 4: return compress_p<4>(a, round_scale, s);
-    case 8: return compress_p<8>(a, round_scale, s);
-    case 16: return compress_p<16>(a, round_scale, s);
+    case 1: return compress_p<1>(a, round_scale, use_pdl, s);
+    case 2: return compress_p<2>(a, round_scale, use_pdl, s);
+    case 4: return compress_p<4>(a, round_scale, use_pdl, s);
+    case 8: return compress_p<8>(a, round_scale, use_pdl, s);
+    case 16: return compress_p<16>(a, round_scale, use_pdl, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_kpool_decode_update(const KpoolDecodeArgs& a, int P, bool round_scale,
-                                       cudaStream_t s) {
+                                       bool use_pdl, cudaStream_t s) {
   switch (P) {
-    case 1: return decode_p<1>(a, round_scale, s);
-    case 2: return decode_p<2>(a, round_scale, s);
-    case 4: return decode_p<4>(a, round_scale, s);
-    case 8: return decode_p<8>(a, round_scale, s);
-    case 16: return decode_p<16>(a, round_scale, s);
+    case 1: return decode_p<1>(a, round_scale, use_pdl, s);
+    case 2: return decode_p<2>(a, round_scale, use_pdl, s);
+    case 4: return decode_p<4>(a, round_scale, use_pdl, s);
+    case 8: return decode_p<8>(a, round_scale, use_pdl, s);
+    case 16: return decode_p<16>(a, round_scale, use_pdl, s);
     default: return cudaErrorInvalidValue;
   }
 }

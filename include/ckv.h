@@ -125,6 +125,8 @@ int32_t ckv_abi_version(void);
  *                   device, nullable, [B*N][D]: the fp32 pooled row, its bf16
  *                   rounding and the bf16 rotated row of every closing token
  *                   (row idx); rows of other tokens are not written.
+ * use_pdl           nonzero: launch as a programmatic dependent launch (the kernel
+ *                   waits for the preceding grid before it touches memory).
  */
 ckv_status ckv_kpool_decode_update(uint8_t* kv_cache, int64_t num_pages, int32_t page_size,
                                    uint16_t* tail_ring, int64_t num_tail_blocks,
@@ -134,8 +136,8 @@ ckv_status ckv_kpool_decode_update(uint8_t* kv_cache, int64_t num_pages, int32_t
                                    const uint16_t* score, int64_t score_stride_b,
                                    int64_t score_stride_t, const float* ape, int32_t B, int32_t N,
                                    int32_t P, int32_t D, int32_t round_scale, float* tap_x,
-                                   uint16_t* tap_xb, uint16_t* tap_yb, int32_t* err_word,
-                                   void* stream);
+                                   uint16_t* tap_xb, uint16_t* tap_yb, int32_t use_pdl,
+                                   int32_t* err_word, void* stream);
 
 /*
  * One-shot pooled compression (vLLM kpool_compress page,
@@ -152,13 +154,14 @@ ckv_status ckv_kpool_decode_update(uint8_t* kv_cache, int64_t num_pages, int32_t
  *                    [n_pools] fp32 scales of every pool ("return compressed").
  * At least one of write_cache / out_fp8 must be requested.
  * tap_x, tap_xb, tap_yb: device, nullable, [n_pools][D] stage taps.
+ * use_pdl            as for ckv_kpool_decode_update.
  */
 ckv_status ckv_kpool_compress(uint8_t* kv_cache, int64_t num_pages, int32_t page_size,
                               const uint16_t* slot_k, const uint16_t* slot_score, const float* ape,
                               const int64_t* loc, const uint8_t* write_mask, int32_t write_cache,
                               uint8_t* out_fp8, float* out_scale, int64_t n_pools, int32_t P,
                               int32_t D, int32_t round_scale, float* tap_x, uint16_t* tap_xb,
-                              uint16_t* tap_yb, int32_t* err_word, void* stream);
+                              uint16_t* tap_yb, int32_t use_pdl, int32_t* err_word, void* stream);
 
 /*
  * Seed the pooled tail ring from a prefill batch (vLLM kpool_compress page,

@@ -62,17 +62,17 @@ def test_validation_rejects_before_launch(lib):
                                        None, None) == 1
     # kpool: D must be 128, P a power of two <= 16, something must be requested
     assert lib.ckv_kpool_compress(one, 1, 16, one, one, one, one, None, 1, None, None, 4, 16, 64, 1,
-                                  None, None, None, None, None) == 2
+                                  None, None, None, 0, None, None) == 2
     assert lib.ckv_kpool_compress(one, 1, 16, one, one, one, one, None, 1, None, None, 4, 3, 128, 1,
-                                  None, None, None, None, None) == 2
+                                  None, None, None, 0, None, None) == 2
     assert lib.ckv_kpool_compress(one, 1, 16, one, one, one, one, None, 0, None, None, 4, 16, 128, 1,
-                                  None, None, None, None, None) == 2
+                                  None, None, None, 0, None, None) == 2
     assert lib.ckv_kpool_compress(one, 1, 16, one, one, one, one, one, 1, one, one, 4, 16, 128, 1,
-                                  None, None, None, None, None) == 2  # mask + returned rows
+                                  None, None, None, 0, None, None) == 2  # mask + returned rows
     assert lib.ckv_kpool_decode_update(one, 1, 16, one, 1, one, one, one, one, 512, 100, one, 512, 128, one,
-                                       2, 4, 16, 128, 1, None, None, None, None, None) == 4  # stride not 16 B
+                                       2, 4, 16, 128, 1, None, None, None, 0, None, None) == 4  # stride not 16 B
     assert lib.ckv_kpool_decode_update(one, 1, 16, one, 1, one, one, one, one, 512, 128, one, 512, 128, one,
-                                       0, 4, 16, 128, 1, None, None, None, None, None) == 0  # empty batch
+                                       0, 4, 16, 128, 1, None, None, None, 0, None, None) == 0  # empty batch
     assert lib.ckv_kpool_seed_tail(one, 1, one, one, one, 5, 16, 96, None, None) == 2
 
 
