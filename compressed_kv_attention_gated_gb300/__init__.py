@@ -8,11 +8,13 @@ from .ckv import (  # noqa: F401
     CkvError,
     ckv_c128_online_decode,
     ckv_c128_online_prefill,
+    ckv_c128_online_prefill_counted,
     ckv_c128_prefill_set_variant,
     ckv_kpool_compress,
     ckv_kpool_compress_set_variant,
     ckv_kpool_decode_update,
     ckv_kpool_seed_tail,
     ckv_plan_online_prefill,
+    ckv_plan_online_prefill_device,
     load,
 )

@@ -31,6 +31,8 @@ _STATUS_FUNCS = {
     "ckv_c128_online_decode": 13,
     "ckv_c128_online_prefill": 18,
     "ckv_plan_online_prefill": 9,
+    "ckv_plan_online_prefill_device": 11,
+    "ckv_c128_online_prefill_counted": 17,
 }
 EXPORTED = tuple(_STATUS_FUNCS) + ("ckv_status_string", "ckv_last_cuda_error", "ckv_abi_version",
                                     "ckv_c128_prefill_set_variant", "ckv_kpool_compress_set_variant")
@@ -91,6 +93,15 @@ def load():
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_void_p,
                 ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(ctypes.c_uint32),
                 ctypes.POINTER(ctypes.c_uint32)]
+            L.ckv_plan_online_prefill_device.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_void_p,
+                ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                ctypes.c_void_p]
+            L.ckv_c128_online_prefill_counted.argtypes = [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                ctypes.c_void_p, ctypes.c_void_p]
             L.ckv_status_string.restype = ctypes.c_char_p
             L.ckv_status_string.argtypes = [ctypes.c_int32]
             L.ckv_last_cuda_error.restype = ctypes.c_int32
@@ -301,6 +312,61 @@ def ckv_kpool_compress_set_variant(variant: int) -> int:
     if prev < 0:
         raise ValueError(f"unknown kpool compress variant {variant}")
     return prev
+
+
+def ckv_plan_online_prefill_device(seq_lens, extend_lens, num_tokens, compress_plan=None, write_plan=None,
+                                   counts=None, pad_for_graph=False, use_pdl=False, err_word=None, stream=None):
+    """Device-side planner; see ckv_plan_online_prefill_device in include/ckv.h.
+
+    seq_lens/extend_lens: CUDA int64 tensors [B].  Returns (compress_plan,
+    write_plan, counts) as CUDA tensors (uint8 [num_tokens, 16] x2, int32 [2]);
+    nothing is copied to the host.
+    """
+    L = load()
+    _cuda("ckv_plan_online_prefill_device", seq_lens, extend_lens, compress_plan, write_plan, counts, err_word)
+    _need(seq_lens.dtype == torch.int64 and extend_lens.dtype == torch.int64 and seq_lens.is_contiguous()
+          and extend_lens.is_contiguous() and seq_lens.numel() == extend_lens.numel(),
+          "seq_lens/extend_lens must be contiguous int64 [B]")
+    dev = seq_lens.device
+    if compress_plan is None:
+        compress_plan = torch.empty((num_tokens, PLAN_ENTRY_BYTES), dtype=torch.uint8, device=dev)
+    if write_plan is None:
+        write_plan = torch.empty((num_tokens, PLAN_ENTRY_BYTES), dtype=torch.uint8, device=dev)
+    if counts is None:
+        counts = torch.zeros((2,), dtype=torch.int32, device=dev)
+    for pl in (compress_plan, write_plan):
+        _need(pl.is_contiguous() and pl.numel() * pl.element_size() >= num_tokens * PLAN_ENTRY_BYTES,
+              "plan buffers must hold num_tokens 16-byte rows")
+    _need(counts.numel() >= 2 and counts.element_size() == 4, "counts must be a 4-byte tensor of 2 elements")
+    _check("ckv_plan_online_prefill_device", L.ckv_plan_online_prefill_device(
+        _ptr(seq_lens), _ptr(extend_lens), seq_lens.numel(), int(num_tokens), _ptr(compress_plan),
+        _ptr(write_plan), int(bool(pad_for_graph)), _ptr(counts), int(bool(use_pdl)), _ptr(err_word),
+        _stream(stream, seq_lens)))
+    return compress_plan, write_plan, counts
+
+
+def ckv_c128_online_prefill_counted(state, input, out, ape, indices, compress_plan, write_plan, counts,
+                                    load_indices=None, use_pdl=False, err_word=None, stream=None):
+    """Online c128 prefill with device-resident segment counts; see include/ckv.h."""
+    L = load()
+    _cuda("ckv_c128_online_prefill_counted", state, input, out, ape, indices, load_indices, compress_plan,
+          write_plan, counts, err_word)
+    T = input.shape[0]
+    D = input.shape[1] // 2
+    B = indices.numel()
+    _need(state.dtype == torch.float32 and state.is_contiguous() and state.numel() % (3 * D) == 0,
+          "state must be contiguous float32 [slots, 3, D]")
+    _need(input.is_contiguous() and input.dim() == 2, "input must be contiguous [T, 2D]")
+    _need(out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (T, D), "out must be float32 [T, D]")
+    _need(ape.dtype == torch.float32 and ape.is_contiguous() and tuple(ape.shape) == (128, D), "ape must be float32 [128, D]")
+    _need(indices.dtype == torch.int32 and indices.is_contiguous(), "indices must be int32 [B]")
+    for pl in (compress_plan, write_plan):
+        _need(pl.is_contiguous() and pl.numel() * pl.element_size() >= min(T, T // 128 + B) * PLAN_ENTRY_BYTES,
+              "plan tensors too small")
+    _check("ckv_c128_online_prefill_counted", L.ckv_c128_online_prefill_counted(
+        _ptr(state), state.numel() // (3 * D), _ptr(input), _dtype(input), T, _ptr(out), _ptr(ape), _ptr(indices),
+        _ptr(load_indices), B, _ptr(compress_plan), _ptr(write_plan), _ptr(counts), D, int(bool(use_pdl)),
+        _ptr(err_word), _stream(stream, input)))
 
 
 def ckv_plan_online_prefill(seq_lens, extend_lens, num_tokens=None, pad_for_graph=False,

@@ -131,7 +131,8 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
   pdl_wait();
   const uint32_t plan_id = blockIdx.x / S;
   const int slice = blockIdx.x % S;
-  const uint32_t n_plans = kWrite ? a.num_write : a.num_compress;
+  const uint32_t n_host = kWrite ? a.num_write : a.num_compress;
+  const uint32_t n_plans = a.counts ? min(a.counts[kWrite ? 1 : 0], n_host) : n_host;
   if (plan_id >= n_plans) return;
   const uint4 raw = *reinterpret_cast<const uint4*>(kWrite ? a.write_plan + plan_id
                                                            : a.compress_plan + plan_id);

@@ -3,6 +3,7 @@
 // Every entry point checks its sizes, flags and pointer alignment on the host,
 // fills an argument block and enqueues the kernels on the caller's stream.
 // Nothing is allocated and nothing synchronises.
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 
@@ -231,6 +232,68 @@ ckv_status ckv_c128_online_prefill(float* state, int64_t num_slots, const void* 
   a.B = B;
   return cuda_status(ckv::launch_c128_prefill(a, D, in_dtype, use_pdl != 0,
                                               static_cast<cudaStream_t>(stream)));
+}
+
+ckv_status ckv_c128_online_prefill_counted(float* state, int64_t num_slots, const void* input,
+                                           ckv_dtype in_dtype, int64_t num_tokens, float* out,
+                                           const float* ape, const int32_t* indices,
+                                           const int32_t* load_indices, int32_t B,
+                                           const ckv_plan_entry* compress_plan,
+                                           const ckv_plan_entry* write_plan, const uint32_t* counts,
+                                           int32_t D, int32_t use_pdl, int32_t* err_word,
+                                           void* stream) {
+  if (B < 0 || num_slots < 0 || num_tokens < 0 || num_tokens > static_cast<int64_t>(UINT32_MAX) ||
+      !head_dim_ok(D))
+    return CKV_ERR_SHAPE;
+  if (in_dtype != CKV_F32 && in_dtype != CKV_BF16) return CKV_ERR_DTYPE;
+  if (num_tokens == 0 || B == 0) return CKV_OK;
+  // every compress segment closes a chunk: per request at most extend/128 + 1 of
+  // them, so at most num_tokens/128 + B in total; at most one write segment each
+  const uint64_t max_c = std::min<uint64_t>(static_cast<uint64_t>(num_tokens) / 128 + B,
+                                            static_cast<uint64_t>(num_tokens));
+  const uint64_t max_w = std::min<uint64_t>(B, static_cast<uint64_t>(num_tokens));
+  const uint64_t S = static_cast<uint64_t>(D / 128);
+  if (max_c * S > static_cast<uint64_t>(INT32_MAX)) return CKV_ERR_SHAPE;
+  if (!state || !input || !ape || !indices || !out || !compress_plan || !write_plan || !counts)
+    return CKV_ERR_NULL;
+  if (!aligned(state, 16) || !aligned(input, 16) || !aligned(out, 16) || !aligned(ape, 16) ||
+      !aligned(compress_plan, 16) || !aligned(write_plan, 16) || !aligned(counts, 4))
+    return CKV_ERR_ALIGN;
+  ckv::C128PrefillArgs a{};
+  a.state = state;
+  a.num_slots = num_slots;
+  a.input = input;
+  a.num_tokens = num_tokens;
+  a.out = out;
+  a.ape = ape;
+  a.indices = indices;
+  a.load_indices = load_indices ? load_indices : indices;
+  a.compress_plan = compress_plan;
+  a.write_plan = write_plan;
+  a.counts = counts;
+  a.err = err_word;
+  a.num_compress = static_cast<uint32_t>(max_c);
+  a.num_write = static_cast<uint32_t>(max_w);
+  a.B = B;
+  return cuda_status(ckv::launch_c128_prefill(a, D, in_dtype, use_pdl != 0,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+ckv_status ckv_plan_online_prefill_device(const int64_t* seq_lens, const int64_t* extend_lens,
+                                          uint32_t B, uint32_t num_tokens,
+                                          ckv_plan_entry* compress_plan, ckv_plan_entry* write_plan,
+                                          int32_t pad_for_graph, uint32_t* counts, int32_t use_pdl,
+                                          int32_t* err_word, void* stream) {
+  if (B > 8192) return CKV_ERR_SHAPE;
+  if (!counts) return CKV_ERR_NULL;
+  if (B > 0 && (!seq_lens || !extend_lens)) return CKV_ERR_NULL;
+  if (num_tokens > 0 && (!compress_plan || !write_plan)) return CKV_ERR_NULL;
+  if (!aligned(compress_plan, 16) || !aligned(write_plan, 16) || !aligned(counts, 4) ||
+      !aligned(seq_lens, 8) || !aligned(extend_lens, 8))
+    return CKV_ERR_ALIGN;
+  return cuda_status(ckv::launch_plan_device(seq_lens, extend_lens, B, num_tokens, compress_plan,
+                                             write_plan, pad_for_graph != 0, counts, err_word,
+                                             use_pdl != 0, static_cast<cudaStream_t>(stream)));
 }
 
 ckv_status ckv_plan_online_prefill(const int64_t* seq_lens, const int64_t* extend_lens, uint32_t B,

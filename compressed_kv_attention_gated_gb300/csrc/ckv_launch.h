@@ -84,6 +84,9 @@ struct C128PrefillArgs {
   const int32_t* load_indices;
   const ckv_plan_entry* compress_plan;
   const ckv_plan_entry* write_plan;
+  // nullable: device [2] counts of valid entries (read by the kernels, after
+  // the programmatic-dependency wait), clamped to num_compress / num_write
+  const uint32_t* counts;
   int32_t* err;
   uint32_t num_compress;
   uint32_t num_write;
@@ -108,6 +111,12 @@ cudaError_t launch_c128_prefill_compress_tma(const C128PrefillArgs& a, int D, in
 int prefill_variant();
 // 0 auto, 1 one warp per pool, 2 persistent bulk-copy pipeline (capi.cu).
 int kpool_compress_variant();
+
+// Device planner (planner_device.cu).
+cudaError_t launch_plan_device(const int64_t* seq_lens, const int64_t* extend_lens, uint32_t B,
+                               uint32_t num_tokens, ckv_plan_entry* compress_plan,
+                               ckv_plan_entry* write_plan, bool pad, uint32_t* counts,
+                               int32_t* err, bool use_pdl, cudaStream_t s);
 
 // Host planner (planner.cpp).
 ckv_status plan_online_prefill_host(const int64_t* seq_lens, const int64_t* extend_lens,

@@ -435,8 +435,7 @@ constexpr int64_t kBulkMinPools = 4096;
 template <int P, bool kRound>
 cudaError_t compress_bulk(const KpoolCompressArgs& a, bool use_pdl, cudaStream_t s) {
   auto kern = kpool_compress_bulk_kernel<P, kRound>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       BulkLayout<P>::kBytes);
+  cudaError_t e = set_max_smem_once<kpool_compress_bulk_kernel<P, kRound>>(BulkLayout<P>::kBytes);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;

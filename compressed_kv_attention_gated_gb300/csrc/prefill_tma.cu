@@ -32,6 +32,7 @@
 
 #include "ckv_device.cuh"
 #include "ckv_launch.h"
+#include "ckv_launch_util.cuh"
 #include "ckv_tma.cuh"
 
 namespace ckv {
@@ -146,7 +147,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slice = blockIdx.x % S;
   const uint32_t group = blockIdx.x / S, ngroups = gridDim.x / S;
-  const uint32_t n = a.num_compress;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSt; ++i) {
@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   pdl_wait();
+  const uint32_t n = a.counts ? min(a.counts[0], a.num_compress) : a.num_compress;
   // bias slice, pre-scaled to the log2 domain
   for (int i = threadIdx.x; i < 128 * kCh / 4; i += kThreads) {
     const int j = i / (kCh / 4), c4 = i % (kCh / 4);
@@ -392,7 +393,7 @@ cudaError_t launch_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   auto kern = c128_prefill_tma_kernel<D, InT>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<InT>::kBytes);
+  e = set_max_smem_once<c128_prefill_tma_kernel<D, InT>>(Layout<InT>::kBytes);
   if (e != cudaSuccess) return e;
   const int grid = sms >= S ? (sms / S) * S : S;
   cudaLaunchConfig_t cfg = {};

@@ -274,6 +274,41 @@ ckv_status ckv_plan_online_prefill(const int64_t* seq_lens, const int64_t* exten
                                    ckv_plan_entry* write_plan, int32_t pad_for_graph,
                                    uint32_t* num_compress, uint32_t* num_write);
 
+/*
+ * Device-side planner: the same plans as ckv_plan_online_prefill (sglang
+ * c128_online.cuh page, plan_online_prefill_host), computed by a CUDA kernel
+ * on `stream`, so that planning and the prefill can be enqueued -- or
+ * captured in a CUDA graph -- without a host round trip.
+ * seq_lens, extend_lens  device int64 [B]; B <= 8192.
+ * compress_plan, write_plan device arrays of num_tokens entries (16-byte aligned).
+ * counts                 device uint32 [2]: receives (num_compress, num_write),
+ *                        both num_tokens with pad_for_graph.
+ * Invalid lengths (extend <= 0, extend > seq, seq >= 2^32, sum != num_tokens)
+ * set CKV_DEVERR_PLAN in err_word and write counts (0, 0).
+ */
+ckv_status ckv_plan_online_prefill_device(const int64_t* seq_lens, const int64_t* extend_lens,
+                                          uint32_t B, uint32_t num_tokens,
+                                          ckv_plan_entry* compress_plan, ckv_plan_entry* write_plan,
+                                          int32_t pad_for_graph, uint32_t* counts, int32_t use_pdl,
+                                          int32_t* err_word, void* stream);
+
+/*
+ * ckv_c128_online_prefill with the segment counts read on the device from
+ * `counts` (device uint32 [2] = num_compress, num_write, e.g. written by
+ * ckv_plan_online_prefill_device) instead of passed by the host.  The grids
+ * are sized for the largest possible counts (num_tokens/128 + B compress and B
+ * write segments); the kernels clamp the device counts to those bounds.  All
+ * other arguments as for ckv_c128_online_prefill.
+ */
+ckv_status ckv_c128_online_prefill_counted(float* state, int64_t num_slots, const void* input,
+                                           ckv_dtype in_dtype, int64_t num_tokens, float* out,
+                                           const float* ape, const int32_t* indices,
+                                           const int32_t* load_indices, int32_t B,
+                                           const ckv_plan_entry* compress_plan,
+                                           const ckv_plan_entry* write_plan, const uint32_t* counts,
+                                           int32_t D, int32_t use_pdl, int32_t* err_word,
+                                           void* stream);
+
 #ifdef __cplusplus
 }
 #endif
