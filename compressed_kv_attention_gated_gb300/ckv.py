@@ -33,6 +33,7 @@ _STATUS_FUNCS = {
     "ckv_plan_online_prefill": 9,
     "ckv_plan_online_prefill_device": 11,
     "ckv_c128_online_prefill_counted": 17,
+    "ckv_expand_pools_and_append_tail": 9,
 }
 EXPORTED = tuple(_STATUS_FUNCS) + ("ckv_status_string", "ckv_last_cuda_error", "ckv_abi_version",
                                     "ckv_c128_prefill_set_variant", "ckv_kpool_compress_set_variant")
@@ -102,6 +103,9 @@ def load():
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                 ctypes.c_void_p, ctypes.c_void_p]
+            L.ckv_expand_pools_and_append_tail.argtypes = [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
             L.ckv_status_string.restype = ctypes.c_char_p
             L.ckv_status_string.argtypes = [ctypes.c_int32]
             L.ckv_last_cuda_error.restype = ctypes.c_int32
@@ -236,6 +240,29 @@ def ckv_kpool_seed_tail(tail_ring, key, score, tslot, err_word=None, stream=None
     _check("ckv_kpool_seed_tail", L.ckv_kpool_seed_tail(
         _ptr(tail_ring), tail_ring.shape[0], _ptr(key), _ptr(score), _ptr(tslot), n, P, D,
         _ptr(err_word), _stream(stream, key)))
+
+
+def ckv_expand_pools_and_append_tail(pool_ids, seq_lens, pool_size, out=None, use_pdl=False, stream=None):
+    """Pool -> token index expansion with the tail appended; see include/ckv.h.
+
+    pool_ids: CUDA int32 [rows, n_groups] (last dim contiguous); seq_lens: CUDA
+    int64 [rows].  Returns int32 [rows, n_groups * pool_size + pool_size - 1].
+    """
+    L = load()
+    _cuda("ckv_expand_pools_and_append_tail", pool_ids, seq_lens, out)
+    _need(pool_ids.dtype == torch.int32 and pool_ids.dim() == 2 and pool_ids.stride(1) == 1,
+          "pool_ids must be int32 [rows, n_groups], last dim contiguous")
+    _need(seq_lens.dtype == torch.int64 and seq_lens.is_contiguous(), "seq_lens must be int64 [rows]")
+    rows, groups = pool_ids.shape
+    cols = groups * pool_size + pool_size - 1
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.int32, device=pool_ids.device)
+    _need(out.dtype == torch.int32 and out.is_contiguous() and tuple(out.shape) == (rows, cols),
+          "out must be contiguous int32 [rows, n_groups * P + P - 1]")
+    _check("ckv_expand_pools_and_append_tail", L.ckv_expand_pools_and_append_tail(
+        _ptr(pool_ids), pool_ids.stride(0), _ptr(seq_lens), rows, groups, int(pool_size), _ptr(out),
+        int(bool(use_pdl)), _stream(stream, pool_ids)))
+    return out
 
 
 # ------------------------------------------------------------ online c128

@@ -170,6 +170,25 @@ ckv_status ckv_kpool_seed_tail(uint16_t* tail_ring, int64_t num_tail_blocks, con
   return cuda_status(ckv::launch_kpool_seed_tail(a, P, static_cast<cudaStream_t>(stream)));
 }
 
+ckv_status ckv_expand_pools_and_append_tail(const int32_t* pool_ids, int64_t pool_ids_stride,
+                                           const int64_t* seq_lens, int32_t rows, int32_t n_groups,
+                                           int32_t P, int32_t* out, int32_t use_pdl, void* stream) {
+  if (rows < 0 || n_groups < 0 || P < 1 || P > 1024 || pool_ids_stride < n_groups) return CKV_ERR_SHAPE;
+  const int64_t cols = static_cast<int64_t>(n_groups) * P + P - 1;
+  if (rows == 0 || cols == 0) return CKV_OK;
+  if (cols > static_cast<int64_t>(INT32_MAX) - 256) return CKV_ERR_SHAPE;
+  if (!seq_lens || !out || (n_groups > 0 && !pool_ids)) return CKV_ERR_NULL;
+  ckv::ExpandArgs a{};
+  a.pool_ids = pool_ids;
+  a.stride = pool_ids_stride;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.rows = rows;
+  a.groups = n_groups;
+  a.P = P;
+  return cuda_status(ckv::launch_expand_pools(a, use_pdl != 0, static_cast<cudaStream_t>(stream)));
+}
+
 ckv_status ckv_c128_online_decode(float* state, int64_t num_slots, const void* input,
                                   ckv_dtype in_dtype, float* out, const float* ape,
                                   const int32_t* indices, const int32_t* seq_lens, int32_t B,

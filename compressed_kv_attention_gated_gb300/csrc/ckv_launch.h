@@ -61,6 +61,14 @@ struct KpoolSeedArgs {
   int32_t* err;
 };
 
+struct ExpandArgs {
+  const int32_t* pool_ids;
+  int64_t stride;
+  const int64_t* seq_lens;
+  int32_t* out;
+  int32_t rows, groups, P;
+};
+
 struct C128DecodeArgs {
   float* state;
   int64_t num_slots;
@@ -98,6 +106,7 @@ cudaError_t launch_kpool_compress(const KpoolCompressArgs& a, int P, bool round_
 cudaError_t launch_kpool_decode_update(const KpoolDecodeArgs& a, int P, bool round_scale,
                                        bool use_pdl, cudaStream_t s);
 cudaError_t launch_kpool_seed_tail(const KpoolSeedArgs& a, int P, cudaStream_t s);
+cudaError_t launch_expand_pools(const ExpandArgs& a, bool use_pdl, cudaStream_t s);
 cudaError_t launch_c128_decode(const C128DecodeArgs& a, int D, int in_dtype, bool use_pdl,
                                cudaStream_t s);
 cudaError_t launch_c128_prefill(const C128PrefillArgs& a, int D, int in_dtype, bool use_pdl,

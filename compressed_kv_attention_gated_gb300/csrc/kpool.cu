@@ -443,6 +443,34 @@ cudaError_t compress_bulk(const KpoolCompressArgs& a, bool use_pdl, cudaStream_t
   return launch_ex(kern, dim3(sms), dim3(kBulkWarps * 32), BulkLayout<P>::kBytes, use_pdl, s, a);
 }
 
+// Pool -> token index expansion with the tail appended: one thread per output
+// column; each row's pool ids are read once per P consecutive columns (a warp
+// broadcast) and the int32 row is written fully coalesced.
+constexpr int kExpandThreads = 256;
+
+__global__ void __launch_bounds__(kExpandThreads)
+    expand_pools_kernel(const __grid_constant__ ExpandArgs a) {
+  pdl_wait();
+  const int64_t groups_cols = static_cast<int64_t>(a.groups) * a.P;
+  const int64_t cols = groups_cols + a.P - 1;
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * kExpandThreads + threadIdx.x;
+  if (c >= cols) return;
+  for (int64_t r = blockIdx.y; r < a.rows; r += gridDim.y) {
+    int32_t v;
+    if (c < groups_cols) {
+      const int64_t g = c / a.P;
+      const int64_t id = a.pool_ids[r * a.stride + g];
+      v = id >= 0 ? static_cast<int32_t>(id * a.P + (c - g * a.P)) : -1;
+    } else {
+      const int64_t s = a.seq_lens[r];
+      const int64_t tail_start = (s / a.P) * a.P;
+      const int64_t i = c - groups_cols;
+      v = i < s - tail_start ? static_cast<int32_t>(tail_start + i) : -1;
+    }
+    a.out[r * cols + c] = v;
+  }
+}
+
 template <int P>
 cudaError_t compress_p(const KpoolCompressArgs& a, bool round_scale, bool use_pdl, cudaStream_t s) {
   const int v = kpool_compress_variant();
@@ -493,6 +521,13 @@ cudaError_t launch_kpool_decode_update(const KpoolDecodeArgs& a, int P, bool rou
     case 16: return decode_p<16>(a, round_scale, use_pdl, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_expand_pools(const ExpandArgs& a, bool use_pdl, cudaStream_t s) {
+  const int64_t cols = static_cast<int64_t>(a.groups) * a.P + a.P - 1;
+  const dim3 grid(static_cast<unsigned>((cols + kExpandThreads - 1) / kExpandThreads),
+                  static_cast<unsigned>(a.rows < 65535 ? a.rows : 65535));
+  return launch_ex(expand_pools_kernel, grid, dim3(kExpandThreads), 0, use_pdl, s, a);
 }
 
 cudaError_t launch_kpool_seed_tail(const KpoolSeedArgs& a, int P, cudaStream_t s) {

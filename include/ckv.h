@@ -178,6 +178,22 @@ ckv_status ckv_kpool_seed_tail(uint16_t* tail_ring, int64_t num_tail_blocks, con
                                int32_t P, int32_t D, int32_t* err_word, void* stream);
 
 /*
+ * Pool -> token index expansion with the tail appended (vLLM kpool_compress
+ * page, expand_pools_and_append_tail: the identity path of
+ * expand_pools_to_tokens followed by append_tail_to_topk).  For row r with
+ * s = seq_lens[r] and G = n_groups, out[r] has G*P + P - 1 int32 columns:
+ *   column g*P + o  = pool_ids[r][g] * P + o, or -1 when pool_ids[r][g] < 0;
+ *   column G*P + i  = (s / P) * P + i when i < s % P (the tokens of the
+ *                     unfinished trailing pool), else -1.
+ * pool_ids  device int32, row r at r * pool_ids_stride (>= n_groups) elements.
+ * seq_lens  device int64 [rows], >= 0.     out  device int32 [rows][G*P + P - 1].
+ * P         1..1024 (P = 1 has no tail columns).
+ */
+ckv_status ckv_expand_pools_and_append_tail(const int32_t* pool_ids, int64_t pool_ids_stride,
+                                           const int64_t* seq_lens, int32_t rows, int32_t n_groups,
+                                           int32_t P, int32_t* out, int32_t use_pdl, void* stream);
+
+/*
  * Online c128 decode (sglang c128_online.cuh page, flash_c128_online_decode
  * and run_decode).  For request b: the token sits at chunk position
  * p = (seq_lens[b] - 1) % 128 with logit z = score + ape[p].

@@ -81,6 +81,7 @@ def lib():
                 "ora_c128_prefill": (None, [P(f32), ctypes.c_void_p, ci, i64, P(f32), P(i32), P(i64),
                                             P(i64), ci, ci, P(f64), P(u8), P(f64), P(i32), ci]),
                 "ora_plan_segments": (ci, [P(i64), P(i64), ci, P(u32), P(u32), i64, P(i64), P(i64)]),
+                "ora_expand_pools_and_append_tail": (None, [P(i32), i64, P(i64), ci, ci, ci, P(i32)]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -253,6 +254,17 @@ def kpool_seed_tail(ring, key, score, tslot):
     tslot = np.ascontiguousarray(tslot, np.int32)
     lib().ora_kpool_seed_tail(_p(ring, ctypes.c_uint16), ring.shape[0], _p(key, ctypes.c_uint16),
                               _p(score, ctypes.c_uint16), _p(tslot, ctypes.c_int32), n, P, D)
+
+
+def expand_pools_and_append_tail(pool_ids, seq_lens, P):
+    """[KPOOL] pool -> token index expansion with the tail appended; int32 [rows, G*P + P - 1]."""
+    pool_ids = np.ascontiguousarray(pool_ids, np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, np.int64)
+    rows, groups = pool_ids.shape
+    out = np.empty((rows, groups * P + P - 1), np.int32)
+    lib().ora_expand_pools_and_append_tail(_p(pool_ids, ctypes.c_int32), groups, _p(seq_lens, ctypes.c_int64),
+                                           rows, groups, P, _p(out, ctypes.c_int32))
+    return out
 
 
 # ------------------------------------------------------------- online c128

@@ -392,6 +392,33 @@ void ora_kpool_seed_tail(uint16_t* ring, int64_t num_blocks, const uint16_t* key
   }
 }
 
+// ------------------- pool -> token expansion with tail append --------------
+// [KPOOL] expand_pools_and_append_tail: the identity path of
+// expand_pools_to_tokens followed by append_tail_to_topk.  For row r with
+// sequence length s and pool_len = s / P:
+//   columns [0, G*P): column g*P + o holds pool_ids[r][g] * P + o when the pool
+//     id is valid, else -1 (reading: a pool id is valid when it is >= 0; the
+//     fused routine receives no separate validity mask);
+//   columns [G*P, G*P + P - 1): column G*P + i holds pool_len*P + i when
+//     i < s - pool_len*P (the tokens of the incomplete trailing pool), else -1.
+// Token ids are formed in 64-bit and stored as int32, as the page's casts do.
+void ora_expand_pools_and_append_tail(const int32_t* pool_ids, int64_t stride, const int64_t* seq_lens,
+                                      int rows, int groups, int P, int32_t* out) {
+  const int64_t cols = static_cast<int64_t>(groups) * P + P - 1;
+  for (int r = 0; r < rows; ++r) {
+    int32_t* o = out + r * cols;
+    for (int g = 0; g < groups; ++g) {
+      const int64_t id = pool_ids[r * stride + g];
+      for (int k = 0; k < P; ++k)
+        o[g * P + k] = id >= 0 ? static_cast<int32_t>(id * P + k) : -1;
+    }
+    const int64_t tail_start = (seq_lens[r] / P) * P;
+    const int64_t tail_count = seq_lens[r] - tail_start;
+    for (int i = 0; i < P - 1; ++i)
+      o[static_cast<int64_t>(groups) * P + i] = i < tail_count ? static_cast<int32_t>(tail_start + i) : -1;
+  }
+}
+
 // ------------------- online c128 decode -----------------------------------
 // [C128] flash_c128_online_decode.  The running state of a slot is
 // (max, sum, kv) with kv already normalised, i.e. for the chunk tokens seen so

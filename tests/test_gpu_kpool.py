@@ -377,3 +377,20 @@ def test_kpool_seed_tail_vs_oracle(ck, ora):
     rring = bf16_bits(ring0).copy()
     ora.kpool_seed_tail(rring, bf16_bits(key), bf16_bits(score), tslot.numpy())
     np.testing.assert_array_equal(bf16_bits(ring), rring)
+
+
+# ------------------------------------------------- pool -> token expansion
+@pytest.mark.parametrize("P", [1, 4, 16])
+def test_expand_pools_and_append_tail_vs_oracle(ck, ora, P):
+    """Index work: bit-exact against the oracle (vLLM page kpool_compress,
+    expand_pools_and_append_tail), including invalid pools, strided rows and a
+    row count above the grid's y limit."""
+    g = torch.Generator().manual_seed(P)
+    for rows, groups in ((3, 5), (70000, 2)):
+        full = torch.randint(-1, 5000, (rows, groups + 3), generator=g, dtype=torch.int32)
+        ids = full[:, :groups]  # row stride groups + 3
+        seq = torch.randint(0, 80000, (rows,), generator=g, dtype=torch.int64)
+        out = ck.ckv_expand_pools_and_append_tail(full.cuda()[:, :groups], seq.cuda(), P)
+        torch.cuda.synchronize()
+        ref = ora.expand_pools_and_append_tail(ids.numpy(), seq.numpy(), P)
+        np.testing.assert_array_equal(out.cpu().numpy(), ref)

@@ -571,3 +571,33 @@ def test_segmenter_invariants_brute_force(ora):
                 cover[rid - wl + 1: rid + 1] += 1
         assert np.all(cover == 1)
         assert np.all(np.bincount(w[:, 1], minlength=B) <= 1) if len(w) else True
+
+
+# ---------------------------------------------------- pool -> token expansion
+@pytest.mark.parametrize("case", json.load(open(os.path.join(GOLDEN, "expand_examples.json")))["cases"],
+                         ids=lambda c: c["name"])
+def test_expand_golden(ora, case):
+    out = ora.expand_pools_and_append_tail(np.array(case["pool_ids"]), np.array(case["seq_lens"]), case["P"])
+    assert out.tolist() == case["out"]
+
+
+def test_expand_invariants(ora):
+    rng = np.random.default_rng(30)
+    for P in (1, 2, 4, 16):
+        rows, G = 7, 5
+        ids = rng.integers(-1, 50, (rows, G)).astype(np.int32)
+        seq = rng.integers(0, 900, rows)
+        out = ora.expand_pools_and_append_tail(ids, seq, P)
+        assert out.shape == (rows, G * P + P - 1)
+        for r in range(rows):
+            hist = out[r, :G * P].reshape(G, P)
+            for g in range(G):
+                if ids[r, g] < 0:
+                    assert np.all(hist[g] == -1)
+                else:  # P consecutive ids starting at a multiple of P
+                    assert hist[g, 0] % P == 0 and np.all(np.diff(hist[g]) == 1) and hist[g, 0] // P == ids[r, g]
+            tail = out[r, G * P:]
+            real = tail[tail >= 0]
+            # the tail is exactly the tokens after the last full pool, in order, then -1s
+            assert real.tolist() == list(range((seq[r] // P) * P, seq[r]))
+            assert np.all(tail[len(real):] == -1)
