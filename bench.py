@@ -419,6 +419,16 @@ def _dist():
     return ws, rank, local
 
 
+def replica_seed(rank):
+    """Seed of a rank's replica: ranks process independent requests."""
+    return 1000 * rank
+
+
+def whole_job_value(tokens_per_step, ws, steps, max_elapsed_ms):
+    """Tokens all ranks processed divided by the slowest rank's time (tokens/s)."""
+    return tokens_per_step * ws * steps / (max_elapsed_ms / 1e3)
+
+
 def _max_over_ranks(x, ws, device):
     if ws == 1:
         return x
@@ -589,7 +599,7 @@ def main():
     from compressed_kv_attention_gated_gb300 import build as libbuild
 
     libbuild.build()
-    step = Step(dev, seed=1000 * rank)
+    step = Step(dev, seed=replica_seed(rank))
     nk = len(step.names)
     stream = torch.cuda.Stream(dev)
     torch.cuda.synchronize()
@@ -631,7 +641,7 @@ def main():
     elapsed_ms = _max_over_ranks(elapsed_ms, ws, dev)
     ms_per_step = elapsed_ms / K
     tokens_step = sum(step.tokens)
-    value = tokens_step * ws * K / (elapsed_ms / 1e3)
+    value = whole_job_value(tokens_step, ws, K, elapsed_ms)
     peak, peak_kind = _peaks()
     kernels = {}
     for i, n in enumerate(step.names):
@@ -666,7 +676,7 @@ def main():
         e1.record(stream)
         e1.synchronize()
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1), ws, dev)
-    e2e = {"value": tokens_step * ws * Ke / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(io.h2d_bytes),
+    e2e = {"value": whole_job_value(tokens_step, ws, Ke, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(io.h2d_bytes),
            "d2h_bytes_per_step": int(io.d2h_bytes), "ms_per_step": e2e_ms / Ke, "steps": Ke}
     assert int(step.err.item()) == 0
 

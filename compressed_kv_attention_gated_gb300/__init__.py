@@ -17,5 +17,6 @@ from .ckv import (  # noqa: F401
     ckv_kpool_seed_tail,
     ckv_plan_online_prefill,
     ckv_plan_online_prefill_device,
+    ckv_wait_timeout_selftest,
     load,
 )

@@ -34,6 +34,7 @@ _STATUS_FUNCS = {
     "ckv_plan_online_prefill_device": 11,
     "ckv_c128_online_prefill_counted": 17,
     "ckv_expand_pools_and_append_tail": 9,
+    "ckv_wait_timeout_selftest": 3,
 }
 EXPORTED = tuple(_STATUS_FUNCS) + ("ckv_status_string", "ckv_last_cuda_error", "ckv_abi_version",
                                     "ckv_c128_prefill_set_variant", "ckv_kpool_compress_set_variant")
@@ -106,6 +107,7 @@ def load():
             L.ckv_expand_pools_and_append_tail.argtypes = [
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                 ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
+            L.ckv_wait_timeout_selftest.argtypes = [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p]
             L.ckv_status_string.restype = ctypes.c_char_p
             L.ckv_status_string.argtypes = [ctypes.c_int32]
             L.ckv_last_cuda_error.restype = ctypes.c_int32
@@ -152,6 +154,14 @@ def _dtype(t):
 def _need(cond, msg):
     if not cond:
         raise ValueError(msg)
+
+
+def ckv_wait_timeout_selftest(err_word, limit_us=20000, stream=None):
+    """Run the bounded-wait self-test (see include/ckv.h); err_word: CUDA int32 [1]."""
+    L = load()
+    _cuda("ckv_wait_timeout_selftest", err_word)
+    _check("ckv_wait_timeout_selftest", L.ckv_wait_timeout_selftest(_ptr(err_word), int(limit_us),
+                                                                    _stream(stream, err_word)))
 
 
 # ------------------------------------------------------------ pooled path

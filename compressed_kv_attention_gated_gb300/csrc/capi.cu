@@ -47,6 +47,13 @@ int32_t ckv_kpool_compress_set_variant(int32_t variant) {
 
 int32_t ckv_abi_version(void) { return 1; }
 
+ckv_status ckv_wait_timeout_selftest(int32_t* err_word, uint32_t limit_us, void* stream) {
+  if (!err_word) return CKV_ERR_NULL;
+  if (limit_us == 0 || limit_us > 2000000u) return CKV_ERR_SHAPE;
+  return cuda_status(ckv::launch_wait_timeout_selftest(err_word, static_cast<uint64_t>(limit_us) * 1000u,
+                                                       static_cast<cudaStream_t>(stream)));
+}
+
 int32_t ckv_last_cuda_error(void) { return g_last_cuda_error; }
 
 const char* ckv_status_string(ckv_status s) {

@@ -116,6 +116,7 @@ cudaError_t launch_c128_prefill(const C128PrefillArgs& a, int D, int in_dtype, b
 bool c128_prefill_tma_supported(const C128PrefillArgs& a, int D, int in_dtype);
 cudaError_t launch_c128_prefill_compress_tma(const C128PrefillArgs& a, int D, int in_dtype,
                                              bool use_pdl, cudaStream_t s);
+cudaError_t launch_wait_timeout_selftest(int32_t* err, uint64_t limit_ns, cudaStream_t s);
 // 0 auto, 1 one CTA per segment, 2 TMA pipeline (capi.cu).
 int prefill_variant();
 // 0 auto, 1 one warp per pool, 2 persistent bulk-copy pipeline (capi.cu).

@@ -358,6 +358,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// A wait that nothing will ever satisfy: one thread arms an mbarrier for one
+// arrival that never comes and waits on it with the given limit; the bounded
+// wait must give up, flag CKV_DEVERR_TIMEOUT and return.
+__global__ void wait_timeout_selftest_kernel(int32_t* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  if (!mbar_wait(&bar, 0, limit_ns)) flag_error(err, CKV_DEVERR_TIMEOUT);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -410,6 +421,11 @@ cudaError_t launch_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t launch_wait_timeout_selftest(int32_t* err, uint64_t limit_ns, cudaStream_t s) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(err, limit_ns);
+  return cudaGetLastError();
+}
 
 bool c128_prefill_tma_supported(const C128PrefillArgs& a, int D, int in_dtype) {
   (void)D;

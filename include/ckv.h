@@ -91,6 +91,15 @@ int32_t ckv_last_cuda_error(void);
 int32_t ckv_abi_version(void);
 
 /*
+ * Self-test of the bounded pipeline waits: launches one thread that waits on
+ * an mbarrier nothing will ever complete, with a limit of limit_us
+ * microseconds (1 .. 2,000,000).  The wait must give up and OR
+ * CKV_DEVERR_TIMEOUT into err_word (device int32); the context stays usable.
+ * The kernels' own waits use the same code with a two-second limit.
+ */
+ckv_status ckv_wait_timeout_selftest(int32_t* err_word, uint32_t limit_us, void* stream);
+
+/*
  * Pooled decode / speculative-verify update (vLLM kpool_compress page,
  * _kpool_decode_update_batched_kernel and
  * kpool_decode_update_and_maybe_write_cache_batched).
