@@ -8,17 +8,18 @@
 // to the output row of the segment's last token.
 //
 // Design for sm_103a (memory bound; no dense contraction, no tensor cores):
-//   * persistent: one CTA per SM, each owning a fixed channel slice of the
-//     row (64 fp32 or 128 bf16 channels = 256 B) for all the segments it is
-//     given (plan p, p + G, p + 2G, ...);
+//   * persistent: one CTA per SM, each owning a fixed 128-channel slice of
+//     the row for all the segments it is given (plan p, p + G, p + 2G, ...);
 //   * the slice of the bias table, pre-multiplied by log2(e), is staged in
 //     shared memory once per CTA (128 x slice fp32);
 //   * warp 0 is the producer: one lane walks the same segment sequence and
-//     streams each segment as 64-row boxes of kv and of score with 2-D tiled
+//     streams each segment as 64-row (bf16) or 32-row (fp32) boxes of kv and
+//     of score with 2-D tiled
 //     TMA loads (cp.async.bulk.tensor) into a ring of stages guarded by
 //     full/empty mbarriers; rows past the input are zero-filled by the TMA
 //     unit and masked by the consumers;
-//   * warps 1..8 are consumers: warp w reduces rows [8w, 8w+8) of every stage
+//   * the other warps (8 for bf16, 4 for fp32) are consumers: warp w reduces
+//     rows [8w, 8w+8) of every stage
 //     two-pass in registers (one ex2 per element, log2 domain), keeping a
 //     running (max, sum, weighted sum) per channel; at the end of a segment the
 //     eight partials meet in shared memory (double-buffered, mbarrier
@@ -38,38 +39,47 @@
 namespace ckv {
 namespace {
 
+// Per input type: channels per slice (kCh), channels per consumer lane (kCpl),
+// pipeline stages, consumer warps and rows per stage (the TMA box height; each
+// consumer warp owns 8 rows of every stage).  A stage holds one box of kv and
+// one of score, 16 KB each.
 template <typename InT>
 struct TmaCfg;
 template <>
 struct TmaCfg<float> {
-  static constexpr int kCh = 64;      // channels per slice (256 B per row)
-  static constexpr int kCpl = 2;      // channels per consumer lane
-  static constexpr int kStages = 5;
+  static constexpr int kCh = 128;     // 512 B of a row
+  static constexpr int kCpl = 4;
+  static constexpr int kStages = 4;
+  static constexpr int kCWarps = 4;
+  static constexpr int kRows = 32;
   static constexpr CUtensorMapDataType kType = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
 };
 template <>
 struct TmaCfg<__nv_bfloat16> {
-  static constexpr int kCh = 128;
+  static constexpr int kCh = 128;     // 256 B of a row
   static constexpr int kCpl = 4;
   static constexpr int kStages = 4;
+  static constexpr int kCWarps = 8;
+  static constexpr int kRows = 64;
   static constexpr CUtensorMapDataType kType = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 };
 
-constexpr int kRows = 64;                        // rows per stage (TMA box height)
-constexpr int kCWarps = 8;                       // consumer warps
-constexpr int kRowsPerWarp = kRows / kCWarps;    // 8
-constexpr int kThreads = (kCWarps + 1) * 32;     // + the producer warp
-constexpr int kBoxBytes = kRows * 256;           // one array, one stage
+constexpr int kRowsPerWarp = 8;
 
 template <typename InT>
 struct Layout {
   static constexpr int kCh = TmaCfg<InT>::kCh, kSt = TmaCfg<InT>::kStages;
+  static constexpr int kCWarps = TmaCfg<InT>::kCWarps, kRows = TmaCfg<InT>::kRows;
+  static constexpr int kRowBytes = kCh * static_cast<int>(sizeof(InT));
+  static constexpr int kBoxBytes = kRows * kRowBytes;                 // one array, one stage
+  static constexpr int kThreads = (kCWarps + 1) * 32;                 // + the producer warp
   static constexpr int kKv = 0;
   static constexpr int kSc = kKv + kSt * kBoxBytes;
   static constexpr int kApe = kSc + kSt * kBoxBytes;                  // [128][kCh] fp32 * log2(e)
   static constexpr int kPart = kApe + 128 * kCh * 4;                  // [2][kCWarps][3][kCh] fp32
   static constexpr int kBar = kPart + 2 * kCWarps * 3 * kCh * 4;     // full[kSt] empty[kSt] ready[2]
   static constexpr int kBytes = kBar + (2 * kSt + 2) * 8;
+  static_assert(kRows == kCWarps * kRowsPerWarp, "each consumer warp owns 8 rows of a stage");
 };
 
 struct Seg {
@@ -99,10 +109,12 @@ template <typename InT>
 struct Row;  // kCpl channels of one smem row, widened to fp32
 template <>
 struct Row<float> {
-  static __device__ __forceinline__ void load(const uint8_t* row, int lane, float (&v)[2]) {
-    const float2 x = reinterpret_cast<const float2*>(row)[lane];
+  static __device__ __forceinline__ void load(const uint8_t* row, int lane, float (&v)[4]) {
+    const float4 x = reinterpret_cast<const float4*>(row)[lane];
     v[0] = x.x;
     v[1] = x.y;
+    v[2] = x.z;
+    v[3] = x.w;
   }
 };
 template <>
@@ -132,11 +144,13 @@ __device__ __forceinline__ void load_ape(const float* ape_row, int lane, float (
 }
 
 template <int D, typename InT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Layout<InT>::kThreads, 1)
     c128_prefill_tma_kernel(const __grid_constant__ CUtensorMap tmap,
                             const __grid_constant__ C128PrefillArgs a) {
   using L = Layout<InT>;
   constexpr int kCh = TmaCfg<InT>::kCh, kCpl = TmaCfg<InT>::kCpl, kSt = TmaCfg<InT>::kStages;
+  constexpr int kCWarps = L::kCWarps, kRows = L::kRows, kBoxBytes = L::kBoxBytes;
+  constexpr int kThreads = L::kThreads, kRowBytes = L::kRowBytes;
   constexpr int S = D / kCh;
   extern __shared__ __align__(1024) uint8_t smem[];
   float* s_ape = reinterpret_cast<float*>(smem + L::kApe);
@@ -253,8 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r0 = static_cast<int>(k) * kRows + cw * kRowsPerWarp;  // first row of this warp
       const int nvalid = min(kRowsPerWarp, max(0, static_cast<int>(s.window) - r0));
       if (nvalid > 0) {
-        const uint8_t* kvb = smem + L::kKv + st * kBoxBytes + cw * kRowsPerWarp * 256;
-        const uint8_t* scb = smem + L::kSc + st * kBoxBytes + cw * kRowsPerWarp * 256;
+        const uint8_t* kvb = smem + L::kKv + st * kBoxBytes + cw * kRowsPerWarp * kRowBytes;
+        const uint8_t* scb = smem + L::kSc + st * kBoxBytes + cw * kRowsPerWarp * kRowBytes;
         const float* apb = s_ape + (chunk_offset + r0) * kCh;
         float z[kRowsPerWarp][kCpl], kv[kRowsPerWarp][kCpl];
         float bm[kCpl];
@@ -264,8 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int r = 0; r < kRowsPerWarp; ++r) {
             float sc[kCpl], ap[kCpl];
-            Row<InT>::load(kvb + r * 256, lane, kv[r]);
-            Row<InT>::load(scb + r * 256, lane, sc);
+            Row<InT>::load(kvb + r * kRowBytes, lane, kv[r]);
+            Row<InT>::load(scb + r * kRowBytes, lane, sc);
             load_ape<kCpl>(apb + r * kCh, lane, ap);
 #pragma unroll
             for (int c = 0; c < kCpl; ++c) {
@@ -278,8 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = 0; r < kRowsPerWarp; ++r) {
             if (r < nvalid) {
               float sc[kCpl], ap[kCpl];
-              Row<InT>::load(kvb + r * 256, lane, kv[r]);
-              Row<InT>::load(scb + r * 256, lane, sc);
+              Row<InT>::load(kvb + r * kRowBytes, lane, kv[r]);
+              Row<InT>::load(scb + r * kRowBytes, lane, sc);
               load_ape<kCpl>(apb + r * kCh, lane, ap);
 #pragma unroll
               for (int c = 0; c < kCpl; ++c) {
@@ -392,7 +406,7 @@ cudaError_t launch_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
   CUtensorMap map;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(2 * D), static_cast<cuuint64_t>(a.num_tokens)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(2 * D * sizeof(InT))};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(Cfg::kCh), static_cast<cuuint32_t>(kRows)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(Cfg::kCh), static_cast<cuuint32_t>(Cfg::kRows)};
   const cuuint32_t estr[2] = {1, 1};
   if (fn(&map, Cfg::kType, 2, const_cast<void*>(a.input), dims, strides, box, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -409,7 +423,7 @@ cudaError_t launch_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
   const int grid = sms >= S ? (sms / S) * S : S;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(Layout<InT>::kThreads);
   cfg.dynamicSmemBytes = Layout<InT>::kBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
