@@ -266,10 +266,9 @@ cudaError_t prefill_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
   if (a.num_compress) {
     const int v = prefill_variant();
     cudaError_t e = cudaErrorNotSupported;
-    // Automatic choice: the TMA pipeline for bf16 inputs with enough segments to
-    // amortise its per-CTA set-up; fp32 inputs measured faster on one CTA per
-    // segment (16-byte vector loads of 128-channel slices).
-    const bool tma = v == 2 || (v == 0 && dtype == CKV_BF16 && a.num_compress >= kTmaMinSegments);
+    // Automatic choice: the TMA pipeline when there are enough segments to
+    // amortise its per-CTA set-up (bias staging, pipeline fill).
+    const bool tma = v == 2 || (v == 0 && a.num_compress >= kTmaMinSegments);
     if (tma && c128_prefill_tma_supported(a, D, dtype)) {
       e = launch_c128_prefill_compress_tma(a, D, dtype, use_pdl, s);
       if (e == cudaErrorNotSupported) (void)cudaGetLastError();

@@ -14,7 +14,7 @@
 //   * exact two-pass softmax from registers: z = score + ape for the P slots,
 //     max, then one ex2 per element;
 //   * for large batches, a persistent variant in which every warp streams its
-//     pools through a private two-stage ring of shared-memory buffers with 1-D
+//     pools through a private three-stage ring of shared-memory buffers with 1-D
 //     bulk copies (cp.async.bulk, completion on an mbarrier), so the next
 //     pool's 8 KB arrive while the current one is reduced, rotated and packed;
 //   * Hadamard-128: two butterfly spans inside the lane (1, 2), then five
@@ -220,14 +220,12 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
 // One-shot pooled compression, persistent and bulk-copy fed.  Warp g (of W in
 // the grid) handles pools g, g + W, g + 2W, ...; each pool's P key rows and P
 // score rows (contiguous, P * 256 B each) are copied into one of the warp's
-// kBulkStages shared-memory stages by lane 0, and the whole warp waits on the
-// stage's mbarrier before reading it.  Pools masked out by write_mask are
+// kBulkStages shared-memory stages by lane 0 (up to kBulkStages - 1 pools
+// ahead of the one being reduced), and the whole warp waits on the stage's
+// mbarrier before reading it.  Pools masked out by write_mask are
 // neither copied nor computed.  Waits are bounded; a timeout flags
 // CKV_DEVERR_TIMEOUT, drains the warp's own copies and leaves.
-constexpr int kBulkWarps = 12;
-constexpr int kBulkStages = 2;
-
-template <int P>
+template <int P, int kBulkWarps, int kBulkStages>
 struct BulkLayout {
   static constexpr int kPoolBytes = P * kD * 2;  // one array of one pool
   static constexpr int kApe = 0;
@@ -236,10 +234,10 @@ struct BulkLayout {
   static constexpr int kBytes = kBar + kBulkWarps * kBulkStages * 8;
 };
 
-template <int P, bool kRound>
+template <int P, bool kRound, int kBulkWarps, int kBulkStages>
 __global__ void __launch_bounds__(kBulkWarps * 32, 1)
     kpool_compress_bulk_kernel(const __grid_constant__ KpoolCompressArgs a) {
-  using L = BulkLayout<P>;
+  using L = BulkLayout<P, kBulkWarps, kBulkStages>;
   extern __shared__ __align__(128) uint8_t smem[];
   float* s_ape = reinterpret_cast<float*>(smem + L::kApe);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -432,15 +430,16 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
 
 constexpr int64_t kBulkMinPools = 4096;
 
-template <int P, bool kRound>
+template <int P, bool kRound, int W, int S>
 cudaError_t compress_bulk(const KpoolCompressArgs& a, bool use_pdl, cudaStream_t s) {
-  auto kern = kpool_compress_bulk_kernel<P, kRound>;
-  cudaError_t e = set_max_smem_once<kpool_compress_bulk_kernel<P, kRound>>(BulkLayout<P>::kBytes);
+  using L = BulkLayout<P, W, S>;
+  auto kern = kpool_compress_bulk_kernel<P, kRound, W, S>;
+  cudaError_t e = set_max_smem_once<kpool_compress_bulk_kernel<P, kRound, W, S>>(L::kBytes);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  return launch_ex(kern, dim3(sms), dim3(kBulkWarps * 32), BulkLayout<P>::kBytes, use_pdl, s, a);
+  return launch_ex(kern, dim3(sms), dim3(W * 32), L::kBytes, use_pdl, s, a);
 }
 
 // Pool -> token index expansion with the tail appended: one thread per output
@@ -474,8 +473,10 @@ __global__ void __launch_bounds__(kExpandThreads)
 template <int P>
 cudaError_t compress_p(const KpoolCompressArgs& a, bool round_scale, bool use_pdl, cudaStream_t s) {
   const int v = kpool_compress_variant();
+  // 8 warps per CTA, each with 3 stages in its ring (measured faster than 12 x 2:
+  // more bytes in flight per warp matter more than more warps)
   if (v == 2 || (v == 0 && a.n_pools >= kBulkMinPools))
-    return round_scale ? compress_bulk<P, true>(a, use_pdl, s) : compress_bulk<P, false>(a, use_pdl, s);
+    return round_scale ? compress_bulk<P, true, 8, 3>(a, use_pdl, s) : compress_bulk<P, false, 8, 3>(a, use_pdl, s);
   const dim3 grid(static_cast<unsigned>((a.n_pools + kWarpsPerCta - 1) / kWarpsPerCta));
   return round_scale
              ? launch_ex(kpool_compress_kernel<P, true>, grid, dim3(kWarpsPerCta * 32), 0, use_pdl, s, a)
