@@ -693,14 +693,16 @@ def main():
     with torch.cuda.stream(stream):
         io.run_step(stream, copy_streams)
         stream.synchronize()
-        # the host link alone: the same H2D bytes, nothing else
-        h0 = torch.cuda.Event(enable_timing=True)
-        h1 = torch.cuda.Event(enable_timing=True)
-        h0.record(stream)
-        io.h2d(stream, copy_streams)
-        h1.record(stream)
-        h1.synchronize()
-        h2d_gbs = io.h2d_bytes / (h0.elapsed_time(h1) / 1e3) / 1e9
+        # the host link alone: the same H2D bytes, nothing else (best of 3)
+        h2d_gbs = 0.0
+        for _ in range(3):
+            h0 = torch.cuda.Event(enable_timing=True)
+            h1 = torch.cuda.Event(enable_timing=True)
+            h0.record(stream)
+            io.h2d(stream, copy_streams)
+            h1.record(stream)
+            h1.synchronize()
+            h2d_gbs = max(h2d_gbs, io.h2d_bytes / (h0.elapsed_time(h1) / 1e3) / 1e9)
         _barrier(ws)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
