@@ -566,6 +566,40 @@ def run_case(args):
             ck.ckv_kpool_decode_update(d["kv_cache"], d["ring"], d["tail_slot_mapping"], d["slot_mapping"],
                                        d["positions"], d["key"], d["score"], d["ape"], err_word=err)
         nbytes = 2048 * 1024
+    elif args.case == "seed_tail":
+        # n prefill tokens over 64 requests, each request's last 16 tokens seeded
+        B = 64
+        per = n // B
+        key = torch.randn((B * per, 128), device=dev).to(torch.bfloat16)
+        score = torch.randn((B * per, 128), device=dev).to(torch.bfloat16)
+        pos = torch.arange(per, device=dev, dtype=torch.int32)
+        tslot = (torch.arange(B, device=dev, dtype=torch.int32)[:, None] * 16 + pos % 16).reshape(-1).contiguous()
+        ring = torch.zeros((B, 2, 16, 128), device=dev, dtype=torch.bfloat16)
+
+        def call():
+            ck.ckv_kpool_seed_tail(ring, key, score, tslot, err_word=err)
+        nbytes = B * 16 * 512 * 2 + tslot.numel() * 8
+    elif args.case == "expand":
+        # n rows of 128 selected pools (P = 16): a top-2048 token selection per row
+        ids = torch.randint(-1, 4096, (n, 128), device=dev, dtype=torch.int32)
+        seq = torch.randint(0, 65536, (n,), device=dev, dtype=torch.int64)
+        out = torch.empty((n, 128 * 16 + 15), device=dev, dtype=torch.int32)
+
+        def call():
+            ck.ckv_expand_pools_and_append_tail(ids, seq, 16, out=out)
+        nbytes = n * (128 * 4 + 8 + (128 * 16 + 15) * 4)
+    elif args.case == "plan_device":
+        # the 64-request prefill batch (prefix U[0,16384], extend U[1,8192]) planned on the device
+        d = synth.c128_prefill("cpu", seed=2, B=64, D=128, max_extend=8192)
+        T = d["num_tokens"]
+        seq, ext = d["seq_lens"].to(dev), d["extend_lens"].to(dev)
+        cp = torch.empty((T, 16), device=dev, dtype=torch.uint8)
+        wp = torch.empty((T, 16), device=dev, dtype=torch.uint8)
+        cnt = torch.zeros((2,), device=dev, dtype=torch.int32)
+
+        def call():
+            ck.ckv_plan_online_prefill_device(seq, ext, T, compress_plan=cp, write_plan=wp, counts=cnt, err_word=err)
+        nbytes = 64 * 16 + (T // 128 + 128) * 16
     else:
         raise SystemExit(f"unknown case {args.case}")
     for _ in range(max(3, args.warmup)):
@@ -585,7 +619,8 @@ def run_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
-                    help="profile one kernel alone: prefill_f32|prefill_bf16|kpool_compress|c128_decode|kpool_decode")
+                    help="profile one kernel alone: prefill_f32|prefill_bf16|kpool_compress|c128_decode|"
+                         "kpool_decode|seed_tail|expand|plan_device")
     ap.add_argument("--case-tokens", type=int, default=131072)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
