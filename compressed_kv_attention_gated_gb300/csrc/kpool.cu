@@ -407,27 +407,37 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   }
 }
 
-// Tail-ring seed: warp w of CTA c handles prefill token c*8 + w.
+// Tail-ring seed: each warp takes 32 consecutive prefill tokens.  Lane j reads
+// the tail slots of token j and of the token P places ahead (two coalesced
+// loads), the warp ballots the tokens that are among their request's last P,
+// and copies each selected token's key and score rows (256 B each) together.
 template <int P>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
     kpool_seed_kernel(const __grid_constant__ KpoolSeedArgs a) {
   const int lane = threadIdx.x & 31;
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
-  if (i >= a.n_tokens) return;
-  const int64_t t = a.tslot[i];
-  if (t < 0) return;
-  const int64_t blk = t / P;
+  const int64_t base = (static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5)) * 32;
+  if (base >= a.n_tokens) return;
+  const int64_t i = base + lane;
+  const int64_t t = i < a.n_tokens ? a.tslot[i] : -1;
   const int64_t ahead = (i + P < a.n_tokens) ? a.tslot[i + P] : -1;
-  if (ahead >= 0 && ahead / P == blk) return;  // not among the request's last P tokens
-  if (blk >= a.num_blocks) {
-    if (lane == 0) flag_error(a.err, CKV_DEVERR_TAIL_BLOCK);
-    return;
+  // a negative ahead slot belongs to no block; otherwise compare blocks (t >= 0 here)
+  const bool tail = t >= 0 && !(ahead >= 0 && ahead / P == t / P);
+  bool ok = true;
+  if (tail && t / P >= a.num_blocks) {
+    flag_error(a.err, CKV_DEVERR_TAIL_BLOCK);
+    ok = false;
   }
-  uint16_t* base = a.ring + blk * 2 * P * kD + (t % P) * kD;
-  reinterpret_cast<uint2*>(base)[lane] = ld_stream_u2(a.key + i * kD + 4 * lane);
-  reinterpret_cast<uint2*>(base + P * kD)[lane] = ld_stream_u2(a.score + i * kD + 4 * lane);
+  uint32_t sel = __ballot_sync(0xFFFFFFFFu, tail && ok);
+  while (sel) {
+    const int j = __ffs(sel) - 1;
+    sel &= sel - 1;
+    const int64_t tj = __shfl_sync(0xFFFFFFFFu, t, j);
+    const int64_t ij = base + j;
+    uint16_t* dst = a.ring + (tj / P) * 2 * P * kD + (tj % P) * kD;
+    reinterpret_cast<uint2*>(dst)[lane] = ld_stream_u2(a.key + ij * kD + 4 * lane);
+    reinterpret_cast<uint2*>(dst + P * kD)[lane] = ld_stream_u2(a.score + ij * kD + 4 * lane);
+  }
 }
-
 constexpr int64_t kBulkMinPools = 4096;
 
 template <int P, bool kRound, int W, int S>
@@ -443,28 +453,33 @@ cudaError_t compress_bulk(const KpoolCompressArgs& a, bool use_pdl, cudaStream_t
 }
 
 // Pool -> token index expansion with the tail appended: one thread per output
-// column; each row's pool ids are read once per P consecutive columns (a warp
-// broadcast) and the int32 row is written fully coalesced.
+// column, looping over rows (the column's group and offset are computed once,
+// with 32-bit arithmetic); each row's pool ids are read once per P
+// consecutive columns (a warp broadcast) and the int32 rows are written fully
+// coalesced.
 constexpr int kExpandThreads = 256;
+constexpr int kExpandRowBlocks = 1024;
 
 __global__ void __launch_bounds__(kExpandThreads)
     expand_pools_kernel(const __grid_constant__ ExpandArgs a) {
   pdl_wait();
-  const int64_t groups_cols = static_cast<int64_t>(a.groups) * a.P;
-  const int64_t cols = groups_cols + a.P - 1;
-  const int64_t c = static_cast<int64_t>(blockIdx.x) * kExpandThreads + threadIdx.x;
+  const uint32_t P = static_cast<uint32_t>(a.P);
+  const uint32_t gcols = static_cast<uint32_t>(a.groups) * P;
+  const uint32_t cols = gcols + P - 1;
+  const uint32_t c = blockIdx.x * kExpandThreads + threadIdx.x;
   if (c >= cols) return;
+  const bool hist = c < gcols;
+  const uint32_t g = hist ? c / P : 0u;
+  const uint32_t o = hist ? c - g * P : c - gcols;
   for (int64_t r = blockIdx.y; r < a.rows; r += gridDim.y) {
     int32_t v;
-    if (c < groups_cols) {
-      const int64_t g = c / a.P;
+    if (hist) {
       const int64_t id = a.pool_ids[r * a.stride + g];
-      v = id >= 0 ? static_cast<int32_t>(id * a.P + (c - g * a.P)) : -1;
+      v = id >= 0 ? static_cast<int32_t>(id * P + o) : -1;
     } else {
       const int64_t s = a.seq_lens[r];
-      const int64_t tail_start = (s / a.P) * a.P;
-      const int64_t i = c - groups_cols;
-      v = i < s - tail_start ? static_cast<int32_t>(tail_start + i) : -1;
+      const int64_t tail_start = s - s % static_cast<int64_t>(P);
+      v = static_cast<int64_t>(o) < s - tail_start ? static_cast<int32_t>(tail_start + o) : -1;
     }
     a.out[r * cols + c] = v;
   }
@@ -493,7 +508,8 @@ cudaError_t decode_p(const KpoolDecodeArgs& a, bool round_scale, bool use_pdl, c
 
 template <int P>
 cudaError_t seed_p(const KpoolSeedArgs& a, cudaStream_t s) {
-  const dim3 grid(static_cast<unsigned>((a.n_tokens + kWarpsPerCta - 1) / kWarpsPerCta));
+  const int64_t per_cta = 32 * kWarpsPerCta;
+  const dim3 grid(static_cast<unsigned>((a.n_tokens + per_cta - 1) / per_cta));
   kpool_seed_kernel<P><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
   return cudaGetLastError();
 }
@@ -527,7 +543,7 @@ cudaError_t launch_kpool_decode_update(const KpoolDecodeArgs& a, int P, bool rou
 cudaError_t launch_expand_pools(const ExpandArgs& a, bool use_pdl, cudaStream_t s) {
   const int64_t cols = static_cast<int64_t>(a.groups) * a.P + a.P - 1;
   const dim3 grid(static_cast<unsigned>((cols + kExpandThreads - 1) / kExpandThreads),
-                  static_cast<unsigned>(a.rows < 65535 ? a.rows : 65535));
+                  static_cast<unsigned>(a.rows < kExpandRowBlocks ? a.rows : kExpandRowBlocks));
   return launch_ex(expand_pools_kernel, grid, dim3(kExpandThreads), 0, use_pdl, s, a);
 }
 
