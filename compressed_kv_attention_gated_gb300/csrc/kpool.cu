@@ -453,12 +453,13 @@ cudaError_t compress_bulk(const KpoolCompressArgs& a, bool use_pdl, cudaStream_t
 }
 
 // Pool -> token index expansion with the tail appended: one thread per output
-// column and 8 rows at a time (the column's group and offset are computed
-// once, with 32-bit arithmetic; the 8 rows' pool ids are loaded before any is
-// used).  Pool ids are read once per P consecutive columns (a warp broadcast)
-// and the int32 rows are written fully coalesced.
+// column, looping over rows (the column's group and offset are computed once,
+// with 32-bit arithmetic; pool ids and lengths go through the read-only path
+// so their loads can run ahead of the previous row's store).  Pool ids are
+// read once per P consecutive columns (a warp broadcast) and the int32 rows are
+// written fully coalesced.
 constexpr int kExpandThreads = 256;
-constexpr int kExpandRows = 8;
+constexpr int kExpandRowBlocks = 1024;
 
 __global__ void __launch_bounds__(kExpandThreads)
     expand_pools_kernel(const __grid_constant__ ExpandArgs a) {
@@ -471,27 +472,17 @@ __global__ void __launch_bounds__(kExpandThreads)
   const bool hist = c < gcols;
   const uint32_t g = hist ? c / P : 0u;
   const uint32_t o = hist ? c - g * P : c - gcols;
-  for (int64_t r0 = static_cast<int64_t>(blockIdx.y) * kExpandRows; r0 < a.rows;
-       r0 += static_cast<int64_t>(gridDim.y) * kExpandRows) {
-    int64_t x[kExpandRows];
-#pragma unroll
-    for (int k = 0; k < kExpandRows; ++k) {
-      const int64_t r = r0 + k;
-      x[k] = r < a.rows ? (hist ? static_cast<int64_t>(a.pool_ids[r * a.stride + g]) : a.seq_lens[r]) : 0;
+  for (int64_t r = blockIdx.y; r < a.rows; r += gridDim.y) {
+    int32_t v;
+    if (hist) {
+      const int64_t id = __ldg(a.pool_ids + r * a.stride + g);
+      v = id >= 0 ? static_cast<int32_t>(id * P + o) : -1;
+    } else {
+      const int64_t s = __ldg(a.seq_lens + r);
+      const int64_t tail_start = s - s % static_cast<int64_t>(P);
+      v = static_cast<int64_t>(o) < s - tail_start ? static_cast<int32_t>(tail_start + o) : -1;
     }
-#pragma unroll
-    for (int k = 0; k < kExpandRows; ++k) {
-      const int64_t r = r0 + k;
-      if (r >= a.rows) break;
-      int32_t v;
-      if (hist) {
-        v = x[k] >= 0 ? static_cast<int32_t>(x[k] * P + o) : -1;
-      } else {
-        const int64_t tail_start = x[k] - x[k] % static_cast<int64_t>(P);
-        v = static_cast<int64_t>(o) < x[k] - tail_start ? static_cast<int32_t>(tail_start + o) : -1;
-      }
-      a.out[r * cols + c] = v;
-    }
+    a.out[r * cols + c] = v;
   }
 }
 
@@ -552,9 +543,8 @@ cudaError_t launch_kpool_decode_update(const KpoolDecodeArgs& a, int P, bool rou
 
 cudaError_t launch_expand_pools(const ExpandArgs& a, bool use_pdl, cudaStream_t s) {
   const int64_t cols = static_cast<int64_t>(a.groups) * a.P + a.P - 1;
-  const int64_t row_blocks = (static_cast<int64_t>(a.rows) + kExpandRows - 1) / kExpandRows;
   const dim3 grid(static_cast<unsigned>((cols + kExpandThreads - 1) / kExpandThreads),
-                  static_cast<unsigned>(row_blocks < 65535 ? row_blocks : 65535));
+                  static_cast<unsigned>(a.rows < kExpandRowBlocks ? a.rows : kExpandRowBlocks));
   return launch_ex(expand_pools_kernel, grid, dim3(kExpandThreads), 0, use_pdl, s, a);
 }
 
