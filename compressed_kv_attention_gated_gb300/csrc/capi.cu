@@ -180,7 +180,8 @@ ckv_status ckv_kpool_seed_tail(uint16_t* tail_ring, int64_t num_tail_blocks, con
 ckv_status ckv_expand_pools_and_append_tail(const int32_t* pool_ids, int64_t pool_ids_stride,
                                            const int64_t* seq_lens, int32_t rows, int32_t n_groups,
                                            int32_t P, int32_t* out, int32_t use_pdl, void* stream) {
-  if (rows < 0 || n_groups < 0 || P < 1 || P > 1024 || pool_ids_stride < n_groups) return CKV_ERR_SHAPE;
+  if (rows < 0 || n_groups < 0 || n_groups > 2048 || P < 1 || P > 1024 || pool_ids_stride < n_groups)
+    return CKV_ERR_SHAPE;
   const int64_t cols = static_cast<int64_t>(n_groups) * P + P - 1;
   if (rows == 0 || cols == 0) return CKV_OK;
   if (cols > static_cast<int64_t>(INT32_MAX) - 256) return CKV_ERR_SHAPE;

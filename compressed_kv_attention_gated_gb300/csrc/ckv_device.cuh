@@ -55,13 +55,6 @@ __device__ __forceinline__ uint2 ld_stream_u2(const void* p) {
                : "l"(p));
   return v;
 }
-__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
-  uint4 v;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
 // Read-only data shared by many CTAs (bias tables): normal caching.
 __device__ __forceinline__ float4 ld_shared_ro_f4(const float* p) {
   return __ldg(reinterpret_cast<const float4*>(p));

@@ -452,37 +452,47 @@ cudaError_t compress_bulk(const KpoolCompressArgs& a, bool use_pdl, cudaStream_t
   return launch_ex(kern, dim3(sms), dim3(W * 32), L::kBytes, use_pdl, s, a);
 }
 
-// Pool -> token index expansion with the tail appended: one thread per output
-// column, looping over rows (the column's group and offset are computed once,
-// with 32-bit arithmetic; pool ids and lengths go through the read-only path
-// so their loads can run ahead of the previous row's store).  Pool ids are
-// read once per P consecutive columns (a warp broadcast) and the int32 rows are
-// written fully coalesced.
-constexpr int kExpandThreads = 256;
-constexpr int kExpandRowBlocks = 1024;
+// Pool -> token index expansion with the tail appended: one warp per row.  The
+// warp copies the row's pool ids into shared memory with one coalesced pass,
+// then writes the row's columns 32 at a time (coalesced int32 stores) with no
+// global load inside the loop; column -> (pool, offset) uses a shift and a
+// mask when P is a power of two, a 32-bit division otherwise.
+constexpr int kExpandWarps = 8;
+constexpr int kExpandMaxGroups = 2048;  // pool ids per row staged in smem (8 KB per warp)
 
-__global__ void __launch_bounds__(kExpandThreads)
+__global__ void __launch_bounds__(kExpandWarps * 32)
     expand_pools_kernel(const __grid_constant__ ExpandArgs a) {
+  extern __shared__ int32_t s_ids[];  // [kExpandWarps][groups]
   pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t P = static_cast<uint32_t>(a.P);
-  const uint32_t gcols = static_cast<uint32_t>(a.groups) * P;
-  const uint32_t cols = gcols + P - 1;
-  const uint32_t c = blockIdx.x * kExpandThreads + threadIdx.x;
-  if (c >= cols) return;
-  const bool hist = c < gcols;
-  const uint32_t g = hist ? c / P : 0u;
-  const uint32_t o = hist ? c - g * P : c - gcols;
-  for (int64_t r = blockIdx.y; r < a.rows; r += gridDim.y) {
-    int32_t v;
-    if (hist) {
-      const int64_t id = __ldg(a.pool_ids + r * a.stride + g);
-      v = id >= 0 ? static_cast<int32_t>(id * P + o) : -1;
-    } else {
-      const int64_t s = __ldg(a.seq_lens + r);
-      const int64_t tail_start = s - s % static_cast<int64_t>(P);
-      v = static_cast<int64_t>(o) < s - tail_start ? static_cast<int32_t>(tail_start + o) : -1;
+  const uint32_t G = static_cast<uint32_t>(a.groups);
+  const uint32_t gcols = G * P, cols = gcols + P - 1;
+  const bool pow2 = (P & (P - 1)) == 0;
+  const uint32_t shift = pow2 ? static_cast<uint32_t>(__ffs(static_cast<int>(P)) - 1) : 0u;
+  int32_t* ids = s_ids + warp * G;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * kExpandWarps + warp; r < a.rows;
+       r += static_cast<int64_t>(gridDim.x) * kExpandWarps) {
+    const int32_t* src = a.pool_ids + r * a.stride;
+    for (uint32_t g = lane; g < G; g += 32) ids[g] = __ldg(src + g);
+    const int64_t s = __ldg(a.seq_lens + r);
+    const int64_t tail_start = s - s % static_cast<int64_t>(P);
+    const int64_t tail_count = s - tail_start;
+    __syncwarp();
+    int32_t* dst = a.out + r * cols;
+    for (uint32_t c = lane; c < cols; c += 32) {
+      int32_t v;
+      if (c < gcols) {
+        const uint32_t g = pow2 ? (c >> shift) : c / P;
+        const int64_t id = ids[g];
+        v = id >= 0 ? static_cast<int32_t>(id * P + (c - g * P)) : -1;
+      } else {
+        const int64_t i = c - gcols;
+        v = i < tail_count ? static_cast<int32_t>(tail_start + i) : -1;
+      }
+      dst[c] = v;
     }
-    a.out[r * cols + c] = v;
+    __syncwarp();
   }
 }
 
@@ -542,10 +552,13 @@ cudaError_t launch_kpool_decode_update(const KpoolDecodeArgs& a, int P, bool rou
 }
 
 cudaError_t launch_expand_pools(const ExpandArgs& a, bool use_pdl, cudaStream_t s) {
-  const int64_t cols = static_cast<int64_t>(a.groups) * a.P + a.P - 1;
-  const dim3 grid(static_cast<unsigned>((cols + kExpandThreads - 1) / kExpandThreads),
-                  static_cast<unsigned>(a.rows < kExpandRowBlocks ? a.rows : kExpandRowBlocks));
-  return launch_ex(expand_pools_kernel, grid, dim3(kExpandThreads), 0, use_pdl, s, a);
+  if (a.groups > kExpandMaxGroups) return cudaErrorInvalidValue;
+  const size_t smem = static_cast<size_t>(kExpandWarps) * a.groups * sizeof(int32_t);
+  cudaError_t e = set_max_smem_once<expand_pools_kernel>(kExpandWarps * kExpandMaxGroups * 4);
+  if (e != cudaSuccess) return e;
+  const int64_t blocks = (static_cast<int64_t>(a.rows) + kExpandWarps - 1) / kExpandWarps;
+  const dim3 grid(static_cast<unsigned>(blocks < (1 << 20) ? blocks : (1 << 20)));
+  return launch_ex(expand_pools_kernel, grid, dim3(kExpandWarps * 32), smem, use_pdl, s, a);
 }
 
 cudaError_t launch_kpool_seed_tail(const KpoolSeedArgs& a, int P, cudaStream_t s) {

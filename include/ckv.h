@@ -194,7 +194,8 @@ ckv_status ckv_kpool_seed_tail(uint16_t* tail_ring, int64_t num_tail_blocks, con
  *   column g*P + o  = pool_ids[r][g] * P + o, or -1 when pool_ids[r][g] < 0;
  *   column G*P + i  = (s / P) * P + i when i < s % P (the tokens of the
  *                     unfinished trailing pool), else -1.
- * pool_ids  device int32, row r at r * pool_ids_stride (>= n_groups) elements.
+ * pool_ids  device int32, row r at r * pool_ids_stride (>= n_groups) elements;
+ *           n_groups <= 2048 (a top-k of up to 2048 * P tokens).
  * seq_lens  device int64 [rows], >= 0.     out  device int32 [rows][G*P + P - 1].
  * P         1..1024 (P = 1 has no tail columns).
  */

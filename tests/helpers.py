@@ -4,7 +4,8 @@ Tolerances (from the accuracy target of the method's deployment):
   * compressed fp32 values (pooled x, c128 kv and sum):
         |gpu - ref| <= 2e-3 * max(1, |ref|)
   * c128 running max: |gpu - ref| <= 2e-3 (absolute)
-  * FP8 codes: within one e4m3 step (ordinal distance <= 1)
+  * FP8 codes and scales: bit-exact where the pooled bf16 row agrees with the
+    oracle's; stage by stage (rotation, quantisation) everywhere
   * scales, ring contents, state-slot selection, cache addresses, plans: exact
 """
 import numpy as np
@@ -43,20 +44,6 @@ def assert_close_abs(gpu, ref, tol=REL_TOL, what=""):
     worst = float(err.max()) if err.size else 0.0
     assert worst <= tol, f"{what}: max abs err {worst:.3e} > {tol}"
     return worst
-
-
-def e4m3_ordinal(codes: np.ndarray) -> np.ndarray:
-    """Map e4m3 codes to integers that increase with the encoded value (+0 == -0)."""
-    c = np.asarray(codes, np.int32)
-    mag = c & 0x7F
-    return np.where(c & 0x80, -mag, mag)
-
-
-def assert_fp8_within_one(gpu_codes, ref_codes, what=""):
-    d = np.abs(e4m3_ordinal(gpu_codes) - e4m3_ordinal(ref_codes))
-    worst = int(d.max()) if d.size else 0
-    assert worst <= 1, f"{what}: FP8 codes differ by {worst} steps"
-    return int((d > 0).sum())
 
 
 def cache_rows(cache: np.ndarray, page_size: int, D: int, locs):

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import (assert_close_rel, assert_fp8_within_one, bf16_bits, cache_rows, f32, u8)
+from helpers import assert_close_rel, bf16_bits, cache_rows, f32, u8
 
 pytestmark = pytest.mark.gpu
 
@@ -36,10 +36,6 @@ def cvariant(request, ck):
     prev = ck.ckv_kpool_compress_set_variant(request.param)
     yield request.param
     ck.ckv_kpool_compress_set_variant(prev)
-
-
-def _to(d, dev):
-    return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
 
 
 _E4M3 = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
