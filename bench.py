@@ -767,7 +767,7 @@ def main():
     assert int(step.err.item()) == 0
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:  # the host baseline is an N = 1 figure
         res, threads, sample = oracle_sample(args.cpu_budget)
         est = cpu_step_estimate(res, step.tokens)
         cpu = {"value": tokens_step / est, "unit": UNIT, "cores": threads, "kind": "oracle",
