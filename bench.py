@@ -150,6 +150,30 @@ class ClockSampler:
                 "reasons": names, "samples": len(self.samples)}
 
 
+# ------------------------------------------------------------ algorithmic bytes
+def kpool_decode_bytes(pd):
+    """(bytes, real tokens, closing pools) of one pooled decode/verify call."""
+    pos = pd["positions"].cpu().numpy()
+    ts = pd["tail_slot_mapping"].cpu().numpy()
+    sm = pd["slot_mapping"].cpu().numpy()
+    P, D = pd["P"], pd["D"]
+    real = int((pos >= 0).sum())
+    stash = int(((pos >= 0) & (ts >= 0)).sum())
+    closes = int(((sm >= 0) & (pos >= 0) & (pos % P == P - 1)).sum())
+    b = real * 2 * D * 2 + pos.size * 12 + stash * 2 * D * 2 + closes * ((P - 1) * 2 * D * 2 + D + 4) + P * D * 4
+    return b, real, closes
+
+
+def c128_decode_bytes(cd):
+    """(bytes, closing requests) of one online c128 decode call."""
+    D = cd["D"]
+    es = cd["input"].element_size()
+    p = (cd["seq_lens"].cpu().numpy().astype(np.int64) - 1) % 128
+    b = cd["B"] * (2 * D * es + 8) + int((p != 0).sum()) * 3 * D * 4 + int((p != 127).sum()) * 3 * D * 4 + \
+        int((p == 127).sum()) * D * 4 + 128 * D * 4
+    return b, int((p == 127).sum())
+
+
 # ------------------------------------------------------------ the workload
 class Step:
     """Device-resident inputs of one step plus the five C-ABI calls."""
@@ -215,18 +239,8 @@ class Step:
     # -- algorithmic bytes and tokens per call ------------------------------
     def _accounting(self):
         pd, cd = self.pd, self.cd
-        pos = pd["positions"].cpu().numpy()
-        ts = pd["tail_slot_mapping"].cpu().numpy()
-        sm = pd["slot_mapping"].cpu().numpy()
-        P, D = pd["P"], pd["D"]
-        real = int((pos >= 0).sum())
-        stash = int(((pos >= 0) & (ts >= 0)).sum())
-        closes = int(((sm >= 0) & (pos >= 0) & (pos % P == P - 1)).sum())
-        b0 = real * 2 * D * 2 + pos.size * 12 + stash * 2 * D * 2 + closes * ((P - 1) * 2 * D * 2 + D + 4) + P * D * 4
-        Dc = cd["D"]
-        p = (cd["seq_lens"].cpu().numpy().astype(np.int64) - 1) % 128
-        b1 = cd["B"] * (2 * Dc * 4 + 8) + int((p != 0).sum()) * 3 * Dc * 4 + int((p != 127).sum()) * 3 * Dc * 4 + \
-            int((p == 127).sum()) * Dc * 4 + 128 * Dc * 4
+        b0, real, closes = kpool_decode_bytes(pd)
+        b1, n_out = c128_decode_bytes(cd)
 
         def prefill_bytes(d, key):
             cpl, wpl = self.plans[key][4], self.plans[key][5]
@@ -249,7 +263,7 @@ class Step:
         b4 = lc["n_pools"] * (2 * lc["P"] * lc["Dp"] * 2 + 8 + lc["Dp"] + 4) + lc["P"] * lc["Dp"] * 4
         self.bytes = [b0, b1, b2, b3, b4]
         self.tokens = [real, cd["B"], self.cp["num_tokens"], lc["num_tokens"], lc["n_pools"] * lc["P"]]
-        self.rows = [closes, int((p == 127).sum()), self.plans["cp"][1], self.plans["lc"][1], lc["n_pools"]]
+        self.rows = [closes, n_out, self.plans["cp"][1], self.plans["lc"][1], lc["n_pools"]]
         self.units = {
             "kpool_decode_update": "per real token 512 B key+score read + 512 B ring stash + 12 B indices; per "
                                    "closing pool 15x512 B ring read + 132 B cache row; + ape 8 KB",
@@ -616,12 +630,112 @@ def run_case(args):
                       "err": int(err.item())}))
 
 
+def run_rotation(args):
+    """Decode calls timed L2-cold and warm, each replayed from one CUDA graph.
+
+    Cold: R independent instances of the batch (R x algorithmic bytes >= 4 x
+    the L2 size), one call on each, captured in order as one graph; every
+    replay is bracketed by events and the median replay time / R is the time of
+    one call that finds none of its data in L2.  Warm: a graph of one call on
+    one instance (its data L2-resident after the first replay).  Both with and
+    without programmatic dependent launch between the captured calls.  The
+    pooled instances share one cache tensor, each writing its own rows
+    (location r * B + b for request b of instance r)."""
+    import math
+
+    import compressed_kv_attention_gated_gb300 as ck
+    from compressed_kv_attention_gated_gb300 import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    err = torch.zeros((1,), dtype=torch.int32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    if args.case == "c128_decode":
+        first = synth.c128_decode(dev, seed=100)
+        nbytes = c128_decode_bytes(first)[0]
+
+        def make(r):
+            return first if r == 0 else synth.c128_decode(dev, seed=100 + r)
+
+        def call(d, pdl):
+            ck.ckv_c128_online_decode(d["state"], d["input"], d["out"], d["ape"], d["indices"], d["seq_lens"],
+                                      use_pdl=pdl, err_word=err)
+    elif args.case == "kpool_decode":
+        first = synth.pooled_decode(dev, seed=100)
+        nbytes = kpool_decode_bytes(first)[0]
+        B, ps = first["B"], first["page_size"]
+        R0 = max(2, math.ceil(4 * l2 / nbytes))
+        cache = torch.zeros(((R0 * B + ps - 1) // ps, ps, first["D"] + 4), device=dev, dtype=torch.uint8)
+
+        def make(r):
+            d = first if r == 0 else synth.pooled_decode(dev, seed=100 + r)
+            sm = d["slot_mapping"]
+            req = torch.arange(B, device=dev, dtype=torch.int32)[:, None].expand_as(sm)
+            d["slot_mapping"] = torch.where(sm >= 0, r * B + req, sm).contiguous()
+            d["kv_cache"] = cache
+            return d
+
+        def call(d, pdl):
+            ck.ckv_kpool_decode_update(d["kv_cache"], d["ring"], d["tail_slot_mapping"], d["slot_mapping"],
+                                       d["positions"], d["key"], d["score"], d["ape"], round_scale=True,
+                                       use_pdl=pdl, err_word=err)
+    else:
+        raise SystemExit("--rotate applies to --case c128_decode or kpool_decode")
+    R = max(2, math.ceil(4 * l2 / nbytes))
+    inst = [make(r) for r in range(R)]
+    peak, peak_kind = _peaks()
+    stream = torch.cuda.Stream(dev)
+    res = {"case": args.case, "mode": "rotate", "instances": R, "l2_bytes": l2, "bytes_per_call": nbytes,
+           "replays": args.steps}
+
+    def timed(graph, n_calls):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t = []
+        with torch.cuda.stream(stream):
+            for _ in range(max(20, args.warmup)):
+                graph.replay()
+            for _ in range(args.steps):
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                e1.synchronize()
+                t.append(e0.elapsed_time(e1) * 1e3 / n_calls)
+        return float(np.median(t))
+
+    for pdl in (True, False):
+        with torch.cuda.stream(stream):
+            for d in inst:
+                call(d, pdl)  # one-time set-up outside the capture
+        stream.synchronize()
+        cold = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cold, stream=stream):
+            for d in inst:
+                call(d, pdl)
+        warm = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(warm, stream=stream):
+            call(inst[0], pdl)
+        tag = "pdl" if pdl else "no_pdl"
+        us_cold = timed(cold, R)
+        us_warm = timed(warm, 1)
+        res[tag] = {"us_per_call_cold": round(us_cold, 3), "gbs_cold": round(nbytes / us_cold / 1e3, 1),
+                    f"frac_of_{peak_kind}_hbm": round(nbytes / us_cold / 1e3 / peak, 4),
+                    "us_single_call_warm": round(us_warm, 3)}
+        del cold, warm
+    torch.cuda.synchronize()
+    res["err"] = int(err.item())
+    res["peak_gbs"] = peak
+    print(json.dumps(res))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
                     help="profile one kernel alone: prefill_f32|prefill_bf16|kpool_compress|c128_decode|"
                          "kpool_decode|seed_tail|expand|plan_device")
     ap.add_argument("--case-tokens", type=int, default=131072)
+    ap.add_argument("--rotate", action="store_true",
+                    help="with --case c128_decode|kpool_decode: L2-cold and warm per-call time from CUDA graph "
+                         "replays over rotating instances (--steps replays, median)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
@@ -645,7 +759,7 @@ def main():
         ck.ckv_c128_prefill_set_variant(args.prefill_variant)
         ck.ckv_kpool_compress_set_variant(args.kpool_variant)
     if args.case:
-        run_case(args)
+        run_rotation(args) if args.rotate else run_case(args)
         return
     ws, rank, local = _dist()
     if ws > 1:

@@ -6,9 +6,10 @@
 // with kv normalised; input row: [2D] = kv | score.
 //
 // Design for sm_103a (memory bound, SIMT, no tensor cores):
-//   decode  -- one warp per request, lane l owning channels 4l + 128c; the
-//              input row is issued before the slot index is known, the slot
-//              state is skipped at chunk position 0; two ex2 per channel.
+//   decode  -- one thread per 4 channels (D / 4 threads per request, the
+//              whole batch resident in one wave); the input row is issued
+//              before the slot index is known, the slot state is skipped at
+//              chunk position 0; two ex2 per channel.
 //   prefill -- one CTA of 8 warps per (segment, 128-channel slice).  Warp w
 //              owns chunk positions [16w, 16w+16), loads them 8 tokens at a
 //              time (16-byte fp32 / 8-byte bf16 vectors, streaming hints) and
@@ -30,85 +31,92 @@ namespace {
 // --------------------------------------------------------------------------
 // decode
 // --------------------------------------------------------------------------
-constexpr int kDecodeWarps = 4;
+constexpr int kDecodeThreads = 256;
+constexpr int kDecodeGroups = 2;     // float4 channel groups per thread
+constexpr int kDecodeMinBlocks = 4;  // CTAs per SM (64 registers, no spills)
 
-template <int D, typename InT>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
+// Thread t of a request owns G groups of 4 channels, 4t + (D / G) g: D / (4G)
+// threads per request and 256 / (D / (4G)) requests per CTA, so the whole
+// decode batch is resident at once and every request's loads are in flight
+// together.
+template <int D, typename InT, int G, int kMinBlocks>
+__global__ void __launch_bounds__(kDecodeThreads, kMinBlocks)
     c128_decode_kernel(const __grid_constant__ C128DecodeArgs a) {
-  constexpr int C = D / 128;  // 4-channel groups per lane
+  constexpr int kTpr = D / (4 * G);             // threads per request
+  constexpr int kRpc = kDecodeThreads / kTpr;   // requests per CTA
+  constexpr int kSpan = D / G;                  // channel distance between groups
   pdl_wait();
   pdl_trigger();
-  const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x * kDecodeWarps + (threadIdx.x >> 5);
+  const int t = threadIdx.x % kTpr;
+  const int b = blockIdx.x * kRpc + threadIdx.x / kTpr;
   if (b >= a.B) return;
 
   // The slot index gates the dependent state loads: issue it before the input stream.
   const int32_t index = a.indices[b];
   const int32_t seq_len = a.seq_lens[b];
+  const int col = 4 * t;
   const InT* in = static_cast<const InT*>(a.input) + static_cast<int64_t>(b) * 2 * D;
-  float4 kin[C], sin_[C];
+  float4 kin[G], sin_[G];
 #pragma unroll
-  for (int c = 0; c < C; ++c) {
-    kin[c] = In4<InT>::load(in, 4 * lane + 128 * c);
-    sin_[c] = In4<InT>::load(in + D, 4 * lane + 128 * c);
+  for (int g = 0; g < G; ++g) {
+    kin[g] = In4<InT>::load(in, col + kSpan * g);
+    sin_[g] = In4<InT>::load(in + D, col + kSpan * g);
   }
   if (seq_len < 1) {
-    if (lane == 0) flag_error(a.err, CKV_DEVERR_SEQ_LEN);
+    if (t == 0) flag_error(a.err, CKV_DEVERR_SEQ_LEN);
     return;
   }
   if (index < 0 || index >= a.num_slots) {
-    if (lane == 0) flag_error(a.err, CKV_DEVERR_SLOT);
+    if (t == 0) flag_error(a.err, CKV_DEVERR_SLOT);
     return;
   }
   const int p = (seq_len - 1) & 127;  // chunk position of the new token
-  float* st = a.state + static_cast<int64_t>(index) * 3 * D;
+  float* st = a.state + static_cast<int64_t>(index) * 3 * D + col;
 
-  float4 ap[C], om[C], os[C], okv[C];
+  float4 ap[G], om[G], os[G], okv[G];
 #pragma unroll
-  for (int c = 0; c < C; ++c) ap[c] = ld_shared_ro_f4(a.ape + p * D + 4 * lane + 128 * c);
+  for (int g = 0; g < G; ++g) ap[g] = ld_shared_ro_f4(a.ape + p * D + col + kSpan * g);
   if (p != 0) {
 #pragma unroll
-    for (int c = 0; c < C; ++c) {
-      const int col = 4 * lane + 128 * c;
-      om[c] = *reinterpret_cast<const float4*>(st + col);
-      os[c] = *reinterpret_cast<const float4*>(st + D + col);
-      okv[c] = *reinterpret_cast<const float4*>(st + 2 * D + col);
+    for (int g = 0; g < G; ++g) {
+      om[g] = *reinterpret_cast<const float4*>(st + kSpan * g);
+      os[g] = *reinterpret_cast<const float4*>(st + D + kSpan * g);
+      okv[g] = *reinterpret_cast<const float4*>(st + 2 * D + kSpan * g);
     }
   }
-  float4 nm[C], ns[C], nkv[C];
+  float4 nm[G], ns[G], nkv[G];
 #pragma unroll
-  for (int c = 0; c < C; ++c) {
+  for (int g = 0; g < G; ++g) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float z = get(sin_[c], i) + get(ap[c], i);
-      const float k = get(kin[c], i);
+      const float z = get(sin_[g], i) + get(ap[g], i);
+      const float k = get(kin[g], i);
       if (p == 0) {
-        set(nm[c], i, z);
-        set(ns[c], i, 1.f);
-        set(nkv[c], i, k);
+        set(nm[g], i, z);
+        set(ns[g], i, 1.f);
+        set(nkv[g], i, k);
       } else {
-        const float m1 = get(om[c], i);
+        const float m1 = get(om[g], i);
         const float M = fmaxf(m1, z);
-        const float w1 = get(os[c], i) * exp_diff(m1, M);
+        const float w1 = get(os[g], i) * exp_diff(m1, M);
         const float w2 = exp_diff(z, M);
         const float s = w1 + w2;
-        set(nm[c], i, M);
-        set(ns[c], i, s);
-        set(nkv[c], i, (get(okv[c], i) * w1 + k * w2) / s);
+        set(nm[g], i, M);
+        set(ns[g], i, s);
+        set(nkv[g], i, (get(okv[g], i) * w1 + k * w2) / s);
       }
     }
   }
   if (p == 127) {
-    float* o = a.out + static_cast<int64_t>(b) * D;
+    float* o = a.out + static_cast<int64_t>(b) * D + col;
 #pragma unroll
-    for (int c = 0; c < C; ++c) reinterpret_cast<float4*>(o + 128 * c)[lane] = nkv[c];
+    for (int g = 0; g < G; ++g) *reinterpret_cast<float4*>(o + kSpan * g) = nkv[g];
   } else {
 #pragma unroll
-    for (int c = 0; c < C; ++c) {
-      const int col = 4 * lane + 128 * c;
-      *reinterpret_cast<float4*>(st + col) = nm[c];
-      *reinterpret_cast<float4*>(st + D + col) = ns[c];
-      *reinterpret_cast<float4*>(st + 2 * D + col) = nkv[c];
+    for (int g = 0; g < G; ++g) {
+      *reinterpret_cast<float4*>(st + kSpan * g) = nm[g];
+      *reinterpret_cast<float4*>(st + D + kSpan * g) = ns[g];
+      *reinterpret_cast<float4*>(st + 2 * D + kSpan * g) = nkv[g];
     }
   }
 }
@@ -253,8 +261,10 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
 
 template <int D, typename InT>
 cudaError_t decode_d(const C128DecodeArgs& a, bool use_pdl, cudaStream_t s) {
-  const dim3 grid((a.B + kDecodeWarps - 1) / kDecodeWarps);
-  return launch_ex(c128_decode_kernel<D, InT>, grid, dim3(kDecodeWarps * 32), 0, use_pdl, s, a);
+  constexpr int G = kDecodeGroups, kRpc = kDecodeThreads / (D / (4 * G));
+  const dim3 grid((a.B + kRpc - 1) / kRpc);
+  return launch_ex(c128_decode_kernel<D, InT, G, kDecodeMinBlocks>, grid, dim3(kDecodeThreads), 0, use_pdl, s,
+                   a);
 }
 
 constexpr uint32_t kTmaMinSegments = 32;
