@@ -19,6 +19,9 @@ std::atomic<int32_t> g_kpool_compress_variant{0};
 ckv_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return CKV_OK;
   g_last_cuda_error = static_cast<int32_t>(e);
+  // a failed launch also leaves its error pending in the runtime; take it so
+  // that it is not reported again by the next call's launch check
+  (void)cudaGetLastError();
   return CKV_ERR_CUDA;
 }
 

@@ -437,8 +437,7 @@ cudaError_t launch_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_wait_timeout_selftest(int32_t* err, uint64_t limit_ns, cudaStream_t s) {
-  wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(err, limit_ns);
-  return cudaGetLastError();
+  return launch_ex(wait_timeout_selftest_kernel, dim3(1), dim3(32), 0, false, s, err, limit_ns);
 }
 
 bool c128_prefill_tma_supported(const C128PrefillArgs& a, int D, int in_dtype) {

@@ -353,22 +353,53 @@ def test_kpool_decode_bad_block_flags(ck):
     assert np.all(r[0, 0, 4] == 0x3F80) and np.all(r[0, 0, 3] == 0)
 
 
-def test_kpool_seed_tail_vs_oracle(ck, ora):
-    P = 16
-    lens = [37, 5, 16, 0, 130]
-    g = torch.Generator().manual_seed(5)
+def _seed_case(P, lens, seed):
+    g = torch.Generator().manual_seed(seed)
     blocks = torch.randperm(len(lens), generator=g)
-    ts = []
+    ts, first = [], []
     for r, n in enumerate(lens):
         ts.append(blocks[r] * P + torch.arange(n) % P)
+        first.append(torch.arange(n) < P)
     tslot = torch.cat(ts).to(torch.int32)
-    tslot[7] = -1  # a padded entry
     n = tslot.numel()
+    # padded entries only among a request's first P tokens: a padded entry
+    # further in would make the token P places before it a tail token too, and
+    # two tokens would write one ring slot (a race the method leaves undefined)
+    pad = (torch.rand((n,), generator=g) < 0.05) & torch.cat(first)
+    tslot[pad] = -1
     key = torch.randn((n, D), generator=g).to(torch.bfloat16)
     score = torch.randn((n, D), generator=g).to(torch.bfloat16)
     ring0 = torch.randn((len(lens), 2, P, D), generator=g).to(torch.bfloat16)
+    return tslot, key, score, ring0
+
+
+def test_kpool_seed_tail_vs_oracle(ck, ora):
+    P = 16
+    tslot, key, score, ring0 = _seed_case(P, [37, 5, 16, 0, 130], 5)
     ring = ring0.cuda()
     ck.ckv_kpool_seed_tail(ring, key.cuda(), score.cuda(), tslot.cuda())
+    torch.cuda.synchronize()
+    rring = bf16_bits(ring0).copy()
+    ora.kpool_seed_tail(rring, bf16_bits(key), bf16_bits(score), tslot.numpy())
+    np.testing.assert_array_equal(bf16_bits(ring), rring)
+
+
+@pytest.mark.parametrize("misaligned", [False, True])
+@pytest.mark.parametrize("P", [1, 2, 4, 8, 16])
+def test_kpool_seed_tail_many_requests(ck, ora, P, misaligned):
+    """Several CTAs of tokens with a ragged end; a slot map that starts 4 bytes
+    past a 16-byte boundary takes the element-wise load path."""
+    r = np.random.default_rng(P)
+    lens = [int(x) for x in r.integers(0, 300, 97)] + [3001, 1, P - 1 if P > 1 else 1]
+    tslot, key, score, ring0 = _seed_case(P, lens, 100 + P)
+    ring = ring0.cuda()
+    ts = tslot.cuda()
+    if misaligned:
+        buf = torch.empty((tslot.numel() + 1,), dtype=torch.int32, device="cuda")
+        buf[1:] = ts
+        ts = buf[1:]
+        assert ts.data_ptr() % 16 != 0
+    ck.ckv_kpool_seed_tail(ring, key.cuda(), score.cuda(), ts)
     torch.cuda.synchronize()
     rring = bf16_bits(ring0).copy()
     ora.kpool_seed_tail(rring, bf16_bits(key), bf16_bits(score), tslot.numpy())
