@@ -136,7 +136,13 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
   __shared__ __align__(16) float4 s_s[kPrefillWarps][32];
   __shared__ __align__(16) float4 s_a[kPrefillWarps][32];
 
-  pdl_wait();
+  // The write pass chained to this call's compress pass reads its plan,
+  // indices and tokens before the dependency wait (none of them is written by
+  // the compress pass, and everything before that pass was complete when it
+  // let this grid launch), so its token reduction overlaps the compress pass;
+  // it waits only before the state.  Otherwise: wait first.
+  const bool early = kWrite && a.write_early;
+  if (!early) pdl_wait();
   const uint32_t plan_id = blockIdx.x / S;
   const int slice = blockIdx.x % S;
   const uint32_t n_host = kWrite ? a.num_write : a.num_compress;
@@ -240,6 +246,7 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
   }
   float kv = acc / ssum;
   const int ch = slice * 128 + t;
+  if (early) pdl_wait();
   if (chunk_offset != 0) {
     const float* ld = a.state + static_cast<int64_t>(load_index) * 3 * D + ch;
     const float m1 = ld[0], s1 = ld[D], k1 = ld[2 * D];
@@ -291,8 +298,10 @@ cudaError_t prefill_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
   }
   if (a.num_write) {
     const dim3 grid(static_cast<unsigned>(a.num_write) * S);
+    C128PrefillArgs w = a;
+    w.write_early = (use_pdl && a.num_compress) ? 1 : 0;
     cudaError_t e =
-        launch_ex(c128_prefill_kernel<D, InT, true>, grid, dim3(kPrefillWarps * 32), 0, use_pdl, s, a);
+        launch_ex(c128_prefill_kernel<D, InT, true>, grid, dim3(kPrefillWarps * 32), 0, use_pdl, s, w);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -99,6 +99,11 @@ struct C128PrefillArgs {
   uint32_t num_compress;
   uint32_t num_write;
   int32_t B;
+  // write pass only, set by the launcher when the write launch is a
+  // programmatic dependent of this call's own compress launch: everything
+  // the write pass reads except the state was final before that launch began,
+  // so the kernel waits for its predecessor only before touching the state
+  int32_t write_early;
 };
 
 cudaError_t launch_kpool_compress(const KpoolCompressArgs& a, int P, bool round_scale,

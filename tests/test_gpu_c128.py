@@ -182,14 +182,17 @@ def test_planner_matches_oracle_segmenter(ck, ora):
         np.testing.assert_array_equal(_plan_rows(wp, nw), rw)
 
 
+@pytest.mark.parametrize("use_pdl", [False, True])
 @pytest.mark.parametrize("D", [128, 256, 512])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_c128_prefill_small(variant, ck, ora, D, dtype):
+def test_c128_prefill_small(variant, ck, ora, D, dtype, use_pdl):
+    """With use_pdl the write pass reads its tokens before waiting for the
+    compress pass, which reads the same state slots the write pass stores."""
     from compressed_kv_attention_gated_gb300 import synth
 
     d = synth.c128_prefill("cpu", seed=D + (dtype == torch.bfloat16), B=9, D=D, max_prefix=500,
                            max_extend=450, dtype=dtype)
-    g_state, g_out, err, _ = _prefill_gpu(ck, d)
+    g_state, g_out, err, _ = _prefill_gpu(ck, d, use_pdl=use_pdl)
     assert err == 0
     nrows, nstates = _check_prefill(ora, d, g_state, g_out)
     assert nrows > 0 and nstates > 0
