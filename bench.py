@@ -385,13 +385,14 @@ class HostIO:
 
 
 # --------------------------------------------------------- CPU oracle sample
-def oracle_sample(budget_s=15.0):
-    """Time the CPU oracle on a bounded sample of each of the five calls and
-    extrapolate to one full step by per-token cost.  Returns (tokens/s, detail)."""
+def oracle_sample(budget_s=15.0, threads=None):
+    """Time the CPU oracle on a bounded sample of each of the five calls (the
+    sample grows with budget_s), on `threads` host threads (default: every
+    core).  Returns (per-call (seconds, tokens), threads, sample description)."""
     import oracle
     from compressed_kv_attention_gated_gb300 import synth
 
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
 
     def bits(t):
         return t.contiguous().view(torch.int16).numpy().view(np.uint16)
@@ -900,6 +901,10 @@ def main():
                "sample": sample,
                "per_call_s": {k: round(v[0], 4) for k, v in res.items()},
                "per_call_tokens": {k: int(v[1]) for k, v in res.items()}}
+        # the same oracle on one thread, on a smaller sample
+        res1, _, sample1 = oracle_sample(max(1.0, args.cpu_budget / 8), threads=1)
+        cpu["single_thread"] = {"value": tokens_step / cpu_step_estimate(res1, step.tokens), "cores": 1,
+                                "sample": sample1}
 
     if rank == 0:
         print(json.dumps({

@@ -35,6 +35,7 @@ _STATUS_FUNCS = {
     "ckv_c128_online_prefill_counted": 17,
     "ckv_expand_pools_and_append_tail": 9,
     "ckv_wait_timeout_selftest": 3,
+    "ckv_check_distinct": 8,
 }
 EXPORTED = tuple(_STATUS_FUNCS) + ("ckv_status_string", "ckv_last_cuda_error", "ckv_abi_version",
                                     "ckv_c128_prefill_set_variant", "ckv_kpool_compress_set_variant")
@@ -108,6 +109,9 @@ def load():
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                 ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
             L.ckv_wait_timeout_selftest.argtypes = [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p]
+            L.ckv_check_distinct.argtypes = [
+                ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
             L.ckv_status_string.restype = ctypes.c_char_p
             L.ckv_status_string.argtypes = [ctypes.c_int32]
             L.ckv_last_cuda_error.restype = ctypes.c_int32
@@ -434,3 +438,22 @@ def ckv_plan_online_prefill(seq_lens, extend_lens, num_tokens=None, pad_for_grap
         _ptr(seq_lens), _ptr(extend_lens), B, num_tokens, _ptr(compress_plan), _ptr(write_plan),
         int(bool(pad_for_graph)), ctypes.byref(nc), ctypes.byref(nw)))
     return compress_plan, write_plan, nc.value, nw.value
+
+
+# ------------------------------------------------------------ contract check
+def ckv_check_distinct(ids, id_range, scratch, err_word, stream=None):
+    """Flag repeated or out-of-range ids; see ckv_check_distinct in include/ckv.h.
+
+    ids: CUDA int32 or int64 tensor (flattened; negative entries ignored);
+    scratch: CUDA int32 tensor of at least ceil(id_range / 32) elements
+    (overwritten); err_word: CUDA int32 [1], CKV_DEVERR_DISTINCT (0x40) is
+    OR-ed into it on a violation.
+    """
+    L = load()
+    _cuda("ckv_check_distinct", ids, scratch, err_word)
+    _need(ids.dtype in (torch.int32, torch.int64) and ids.is_contiguous(), "ids must be contiguous int32/int64")
+    _need(scratch.dtype == torch.int32 and scratch.is_contiguous(), "scratch must be contiguous int32")
+    _need(err_word.dtype == torch.int32, "err_word must be int32")
+    _check("ckv_check_distinct", L.ckv_check_distinct(
+        _ptr(ids), ids.element_size(), ids.numel(), int(id_range), _ptr(scratch), scratch.numel(),
+        _ptr(err_word), _stream(stream, ids)))

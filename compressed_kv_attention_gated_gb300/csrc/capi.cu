@@ -337,4 +337,16 @@ ckv_status ckv_plan_online_prefill(const int64_t* seq_lens, const int64_t* exten
                                        write_plan, pad_for_graph != 0, num_compress, num_write);
 }
 
+ckv_status ckv_check_distinct(const void* ids, int32_t id_bytes, int64_t n, int64_t range,
+                              uint32_t* scratch, int64_t scratch_words, int32_t* err_word,
+                              void* stream) {
+  if ((id_bytes != 4 && id_bytes != 8) || n < 0 || range < 1 || range > (int64_t{1} << 40))
+    return CKV_ERR_SHAPE;
+  if (scratch_words < (range + 31) / 32) return CKV_ERR_SHAPE;
+  if (!scratch || !err_word || (n > 0 && !ids)) return CKV_ERR_NULL;
+  if (!aligned(ids, static_cast<uintptr_t>(id_bytes)) || !aligned(scratch, 4)) return CKV_ERR_ALIGN;
+  return cuda_status(ckv::launch_check_distinct(ids, id_bytes, n, range, scratch, err_word,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -140,4 +140,10 @@ ckv_status plan_online_prefill_host(const int64_t* seq_lens, const int64_t* exte
                                     bool pad_for_graph, uint32_t* num_compress,
                                     uint32_t* num_write);
 
+// validate.cu: clear `bits` (ceil(range / 32) words), then flag repeated or
+// out-of-range non-negative ids of the first n (int32 when id_bytes == 4,
+// else int64).
+cudaError_t launch_check_distinct(const void* ids, int id_bytes, int64_t n, int64_t range, uint32_t* bits,
+                                  int32_t* err, cudaStream_t s);
+
 }  // namespace ckv

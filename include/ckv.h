@@ -60,6 +60,7 @@ typedef int32_t ckv_status;
 #define CKV_DEVERR_PLAN 0x8u       /* plan entry fields inconsistent or out of range */
 #define CKV_DEVERR_SEQ_LEN 0x10u   /* decode seq_len < 1 */
 #define CKV_DEVERR_TIMEOUT 0x20u   /* a pipeline wait gave up after 2 s (never expected) */
+#define CKV_DEVERR_DISTINCT 0x40u  /* ckv_check_distinct: an id repeats or is >= range */
 
 typedef int32_t ckv_dtype;
 #define CKV_F32 0
@@ -334,6 +335,29 @@ ckv_status ckv_c128_online_prefill_counted(float* state, int64_t num_slots, cons
                                            const ckv_plan_entry* write_plan, const uint32_t* counts,
                                            int32_t D, int32_t use_pdl, int32_t* err_word,
                                            void* stream);
+
+/*
+ * Debug check of the caller contract (no counterpart in the sources, which
+ * state the contract and leave it unchecked).  Within one call the kernels
+ * above need distinct state slots (`indices` of the c128 calls), distinct
+ * cache locations (`slot_mapping`, `loc` of the pooled calls) and a tail
+ * block per request that no other request uses; a repeat is a data race that
+ * no kernel detects.  This call checks one such list: it ORs
+ * CKV_DEVERR_DISTINCT into *err_word when one of the first n ids repeats or
+ * is >= range.  Negative ids (padding) are ignored.  For tail blocks, pass one
+ * block id per request.
+ *   ids        device, n int32 (id_bytes = 4) or int64 (id_bytes = 8)
+ *   range      ids are expected in [0, range); 1 <= range <= 2^40
+ *   scratch    device uint32 [scratch_words], scratch_words >= ceil(range/32),
+ *              owned by the caller; cleared and then used as a bitmap (one bit
+ *              per id), so its contents on return are not meaningful
+ *   err_word   device int32, required
+ * Enqueues two kernels (clear, mark) on `stream`.  Calls that share `scratch`
+ * and overlap on the GPU race.  n == 0 clears the scratch and checks nothing.
+ */
+ckv_status ckv_check_distinct(const void* ids, int32_t id_bytes, int64_t n, int64_t range,
+                              uint32_t* scratch, int64_t scratch_words, int32_t* err_word,
+                              void* stream);
 
 #ifdef __cplusplus
 }

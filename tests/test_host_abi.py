@@ -74,6 +74,19 @@ def test_validation_rejects_before_launch(lib):
     assert lib.ckv_kpool_decode_update(one, 1, 16, one, 1, one, one, one, one, 512, 128, one, 512, 128, one,
                                        0, 4, 16, 128, 1, None, None, None, 0, None, None) == 0  # empty batch
     assert lib.ckv_kpool_seed_tail(one, 1, one, one, one, 5, 16, 96, None, None) == 2
+    # distinct-id check: id width, range, scratch size, required pointers, alignment
+    chk = lib.ckv_check_distinct
+    chk.argtypes = [P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, P, ctypes.c_int64, P, P]
+    assert chk(one, 2, 10, 64, one, 2, one, None) == 2       # id_bytes must be 4 or 8
+    assert chk(one, 4, 10, 0, one, 2, one, None) == 2        # empty range
+    assert chk(one, 4, 10, 1 << 41, one, 1 << 36, one, None) == 2  # range above 2^40
+    assert chk(one, 4, 10, 65, one, 2, one, None) == 2       # 65 ids need 3 scratch words
+    assert chk(one, 4, -1, 64, one, 2, one, None) == 2
+    assert chk(one, 4, 10, 64, None, 2, one, None) == 1      # scratch required
+    assert chk(one, 4, 10, 64, one, 2, None, None) == 1      # err_word required
+    assert chk(None, 4, 10, 64, one, 2, one, None) == 1      # ids required when n > 0
+    assert chk(P(18), 4, 10, 64, one, 2, one, None) == 4     # int32 ids 4-byte aligned
+    assert chk(P(20), 8, 10, 64, one, 2, one, None) == 4     # int64 ids 8-byte aligned
 
 
 def _plan(lib, seq, ext, pad=False, num_tokens=None):
