@@ -11,6 +11,7 @@ from .ckv import (  # noqa: F401
     ckv_c128_online_prefill_counted,
     ckv_c128_prefill_set_variant,
     ckv_check_distinct,
+    ckv_check_distinct_noalloc,
     ckv_expand_pools_and_append_tail,
     ckv_kpool_compress,
     ckv_kpool_compress_set_variant,

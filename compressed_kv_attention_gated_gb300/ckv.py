@@ -36,6 +36,7 @@ _STATUS_FUNCS = {
     "ckv_expand_pools_and_append_tail": 9,
     "ckv_wait_timeout_selftest": 3,
     "ckv_check_distinct": 8,
+    "ckv_check_distinct_noalloc": 6,
 }
 EXPORTED = tuple(_STATUS_FUNCS) + ("ckv_status_string", "ckv_last_cuda_error", "ckv_abi_version",
                                     "ckv_c128_prefill_set_variant", "ckv_kpool_compress_set_variant")
@@ -112,6 +113,8 @@ def load():
             L.ckv_check_distinct.argtypes = [
                 ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                 ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+            L.ckv_check_distinct_noalloc.argtypes = [
+                ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
             L.ckv_status_string.restype = ctypes.c_char_p
             L.ckv_status_string.argtypes = [ctypes.c_int32]
             L.ckv_last_cuda_error.restype = ctypes.c_int32
@@ -457,3 +460,20 @@ def ckv_check_distinct(ids, id_range, scratch, err_word, stream=None):
     _check("ckv_check_distinct", L.ckv_check_distinct(
         _ptr(ids), ids.element_size(), ids.numel(), int(id_range), _ptr(scratch), scratch.numel(),
         _ptr(err_word), _stream(stream, ids)))
+
+
+NOALLOC_MAX_RANGE = 1 << 21
+
+
+def ckv_check_distinct_noalloc(ids, id_range, err_word, stream=None):
+    """ckv_check_distinct with the library's own static bitmap (no scratch
+    argument, nothing allocated); for callers that cannot allocate device
+    memory.  id_range must be at most NOALLOC_MAX_RANGE (2^21).  The first call
+    on a device looks up the bitmap's address: make it before any stream
+    capture.  Calls that overlap on the GPU share the bitmap and race."""
+    L = load()
+    _cuda("ckv_check_distinct_noalloc", ids, err_word)
+    _need(ids.dtype in (torch.int32, torch.int64) and ids.is_contiguous(), "ids must be contiguous int32/int64")
+    _need(err_word.dtype == torch.int32, "err_word must be int32")
+    _check("ckv_check_distinct_noalloc", L.ckv_check_distinct_noalloc(
+        _ptr(ids), ids.element_size(), ids.numel(), int(id_range), _ptr(err_word), _stream(stream, ids)))

@@ -146,4 +146,10 @@ ckv_status plan_online_prefill_host(const int64_t* seq_lens, const int64_t* exte
 cudaError_t launch_check_distinct(const void* ids, int id_bytes, int64_t n, int64_t range, uint32_t* bits,
                                   int32_t* err, cudaStream_t s);
 
+// validate.cu: the same check with the bitmap in a static device array of
+// noalloc_check_max_range() bits shared by every call (no allocation).
+int64_t noalloc_check_max_range();
+cudaError_t launch_check_distinct_noalloc(const void* ids, int id_bytes, int64_t n, int64_t range, int32_t* err,
+                                          cudaStream_t s);
+
 }  // namespace ckv

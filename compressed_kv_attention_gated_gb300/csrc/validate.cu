@@ -9,6 +9,7 @@
 // out of range.  Both kernels are grid-stride loops over a grid of a few CTAs
 // per SM.
 #include <cstdint>
+#include <mutex>
 
 #include "ckv_device.cuh"
 #include "ckv_launch.h"
@@ -63,6 +64,49 @@ cudaError_t launch_check_distinct(const void* ids, int id_bytes, int64_t n, int6
                      static_cast<const int32_t*>(ids), n, range, bits, err);
   return launch_ex(mark_distinct_kernel<int64_t>, dim3(grid_for(n, sms)), dim3(kCheckThreads), 0, false, s,
                    static_cast<const int64_t*>(ids), n, range, bits, err);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.  Some callers cannot hand the check a scratch
+// buffer: a serving engine that reserves nearly all HBM for its paged KV cache
+// and owns every byte of it through its own allocator, or a loop that must not
+// call cudaMalloc because cudaMalloc may synchronise the device and stall it.
+// For them the bitmap lives in this file-scope array, which every GPU that
+// loads the library holds until the process exits; every call shares it.  In
+// host code `g_noalloc_bits` is only a host-side stand-in for the symbol, never
+// a device address: the device address is looked up with cudaGetSymbolAddress,
+// once per device, with that device current.
+constexpr int64_t kNoAllocWords = int64_t{1} << 16;  // 256 KB: ids in [0, 2^21)
+static __device__ __align__(256) uint32_t g_noalloc_bits[kNoAllocWords];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+uint32_t* g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+int64_t noalloc_check_max_range() { return kNoAllocWords * 32; }
+
+cudaError_t launch_check_distinct_noalloc(const void* ids, int id_bytes, int64_t n, int64_t range, int32_t* err,
+                                          cudaStream_t s) {
+  if (range > kNoAllocWords * 32) return cudaErrorInvalidValue;  // the entry point rejects this first
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  uint32_t* bits = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_noalloc_bits);
+      if (e != cudaSuccess) return e;
+      g_noalloc_ptr[dev] = static_cast<uint32_t*>(p);
+    }
+    bits = g_noalloc_ptr[dev];
+  }
+  // the clear kernel resets the words this call uses before any id is marked
+  return launch_check_distinct(ids, id_bytes, n, range, bits, err, s);
 }
 
 }  // namespace ckv

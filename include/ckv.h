@@ -359,6 +359,26 @@ ckv_status ckv_check_distinct(const void* ids, int32_t id_bytes, int64_t n, int6
                               uint32_t* scratch, int64_t scratch_words, int32_t* err_word,
                               void* stream);
 
+/*
+ * ckv_check_distinct without a scratch argument, for callers that cannot
+ * allocate device memory: e.g. a serving engine that has reserved nearly all
+ * HBM for its paged KV cache and hands out no other buffers, or a loop that
+ * must not call cudaMalloc because it may synchronise the device.  The paper
+ * has no counterpart.  The bitmap is a static device array of
+ * CKV_NOALLOC_MAX_RANGE bits (256 KB) inside the library, held by every GPU
+ * that loads it until the process exits; the library allocates nothing.
+ *   ids, id_bytes, n, err_word, stream  as for ckv_check_distinct
+ *   range      1 <= range <= CKV_NOALLOC_MAX_RANGE; a larger range returns
+ *              CKV_ERR_SHAPE and launches nothing
+ * The first call on each device looks up the array's device address (with
+ * that device current) and keeps it; make that first call before any stream
+ * capture.  Every call uses the same array: it is cleared at the start of each
+ * call, and calls that overlap on the GPU (other streams, other threads) race.
+ */
+#define CKV_NOALLOC_MAX_RANGE (1 << 21)
+ckv_status ckv_check_distinct_noalloc(const void* ids, int32_t id_bytes, int64_t n, int64_t range,
+                                      int32_t* err_word, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
