@@ -211,6 +211,35 @@ def test_c128_prefill_full_size(variant, ck, ora, use_pdl, pad):
     assert nrows > 1000 and nstates > 30
 
 
+# (prefix, extend) pairs on every chunk boundary: first token of a chunk,
+# last token of a chunk, exactly one chunk, one past it, single tokens, spans
+# of many chunks, and segments ending on position 127 with nothing to write
+BOUNDARY_CASES = [(0, 1), (0, 127), (0, 128), (0, 129), (127, 1), (127, 2), (126, 2), (128, 128), (1, 255),
+                  (255, 1), (256, 384), (100, 28), (100, 29), (383, 1), (0, 1024), (64, 640), (511, 130)]
+
+
+@pytest.mark.parametrize("use_pdl", [False, True])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_c128_prefill_chunk_boundaries(variant, ck, ora, dtype, use_pdl):
+    D = 128
+    B = len(BOUNDARY_CASES)
+    g = torch.Generator().manual_seed(31)
+    pre = torch.tensor([c[0] for c in BOUNDARY_CASES], dtype=torch.int64)
+    ext = torch.tensor([c[1] for c in BOUNDARY_CASES], dtype=torch.int64)
+    T = int(ext.sum())
+    st = torch.zeros((B, 3, D))
+    st[:, 0] = torch.randn((B, D), generator=g)
+    st[:, 1] = 1.0 + 10 * torch.rand((B, D), generator=g)
+    st[:, 2] = torch.randn((B, D), generator=g)
+    d = {"seq_lens": pre + ext, "extend_lens": ext, "input": torch.randn((T, 2 * D), generator=g).to(dtype),
+         "ape": torch.randn((128, D), generator=g) * 0.1, "indices": torch.arange(B, dtype=torch.int32),
+         "num_tokens": T, "D": D, "state": st}
+    g_state, g_out, err, (cp, wp, nc, nw) = _prefill_gpu(ck, d, use_pdl=use_pdl)
+    assert err == 0
+    nrows, nstates = _check_prefill(ora, d, g_state, g_out)
+    assert nc == nrows and nw == nstates
+
+
 def test_c128_prefill_load_indices_differ(variant, ck, ora):
     from compressed_kv_attention_gated_gb300 import synth
 

@@ -41,8 +41,8 @@ def _rows(t, n):
 @pytest.mark.parametrize("pad", [False, True])
 def test_device_planner_matches_host_planner(ck, ora, pad):
     rng = np.random.default_rng(0)
-    for trial in range(40):
-        B = int(rng.integers(1, 40)) if trial < 38 else int(rng.integers(1500, 3000))
+    for trial in range(41):
+        B = int(rng.integers(1, 40)) if trial < 38 else int(rng.integers(1500, 3000)) if trial < 40 else 8192
         ext = rng.integers(1, 700, B)
         pre = rng.integers(0, 900, B)
         seq = torch.from_numpy((pre + ext).astype(np.int64))
