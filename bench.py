@@ -285,21 +285,24 @@ class HostIO:
         self.s = step
         dev = step.dev
         self.pairs = []  # (pinned host tensor, device tensor)
+        self.groups = [[] for _ in range(5)]  # the pairs each call reads, in call order
 
-        def add(t):
+        def add(call, t):
             h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
             h.copy_(t)
             self.pairs.append((h, t))
+            self.groups[call].append((h, t))
 
         pd, cd, cp, lc = step.pd, step.cd, step.cp, step.lc
         for k in ("key", "score", "tail_slot_mapping", "slot_mapping", "positions"):
-            add(pd[k])
+            add(0, pd[k])
         for k in ("input", "indices", "seq_lens"):
-            add(cd[k])
+            add(1, cd[k])
         for k in ("input", "indices"):
-            add(cp[k])
-        for k in ("input", "slot_k", "slot_score", "loc"):
-            add(lc[k])
+            add(2, cp[k])
+        add(3, lc["input"])
+        for k in ("slot_k", "slot_score", "loc"):
+            add(4, lc[k])
         # host planner output goes straight into pinned buffers
         self.plan_host = {}
         for key, d in (("cp", cp), ("lc", lc)):
@@ -363,25 +366,73 @@ class HostIO:
         for cs in copy_streams:
             stream.wait_stream(cs)
 
+    def _issue(self, pairs, copy_streams, rr):
+        """Enqueue the copies of one call's inputs on the copy streams (small
+        tensors round-robin, tensors above 64 MB split in equal byte ranges over
+        all of them); returns the streams used."""
+        big = 64 << 20
+        n = len(copy_streams)
+        used = []
+        for h, dv in pairs:
+            nb = h.numel() * h.element_size()
+            if nb <= big:
+                cs = copy_streams[rr[0] % n]
+                rr[0] += 1
+                with torch.cuda.stream(cs):
+                    dv.copy_(h, non_blocking=True)
+                used.append(cs)
+                continue
+            hb = h.view(-1).view(torch.uint8)
+            db = dv.view(-1).view(torch.uint8)
+            step_b = (nb + n - 1) // n
+            for i, cs in enumerate(copy_streams):
+                lo, hi = i * step_b, min(nb, (i + 1) * step_b)
+                if lo < hi:
+                    with torch.cuda.stream(cs):
+                        db[lo:hi].copy_(hb[lo:hi], non_blocking=True)
+                    used.append(cs)
+        return list({id(c): c for c in used}.values())
+
     def run_step(self, stream=None, copy_streams=()):
+        """One step from host memory: the host planner writes the plans into
+        pinned buffers, every call's inputs are copied in call order on the copy
+        streams, and each call starts as soon as its own inputs have arrived (so
+        it runs under the copies of the calls after it); its results are
+        gathered and read back right after it."""
         s = self.s
         ck = s.ck
-        for key, d in (("cp", s.cp), ("lc", s.lc)):
+        stream = stream or torch.cuda.current_stream()
+        groups = [list(g) for g in self.groups]
+        for call, key, d in ((2, "cp", s.cp), (3, "lc", s.lc)):
             hc, hw = self.plan_host[key]
             _, _, nc, nw = ck.ckv_plan_online_prefill(d["seq_lens"], d["extend_lens"], compress_plan=hc, write_plan=hw)
             dc, _, dw, _ = s.plans[key][:4]
             if nc:
-                dc[:nc].copy_(hc[:nc], non_blocking=True)
+                groups[call].append((hc[:nc], dc[:nc]))
             if nw:
-                dw[:nw].copy_(hw[:nw], non_blocking=True)
-        self.h2d(stream or torch.cuda.current_stream(), list(copy_streams))
+                groups[call].append((hw[:nw], dw[:nw]))
+        cstreams = list(copy_streams) or [stream]
+        for cs in cstreams:
+            cs.wait_stream(stream)  # the previous step's kernels are done with the input buffers
+        ready = []
+        rr = [0]
+        for g in groups:
+            evs = []
+            for cs in self._issue(g, cstreams, rr):
+                ev = torch.cuda.Event()
+                ev.record(cs)
+                evs.append(ev)
+            ready.append(evs)
+        gathers = [lambda: self.outs[0].copy_(s.pd["kv_cache"].view(-1).index_select(0, self.g_pd), non_blocking=True),
+                   lambda: self.outs[1].copy_(s.cd["out"].index_select(0, self.g_cd), non_blocking=True),
+                   lambda: self.outs[2].copy_(s.cp["out"].index_select(0, self.g_cp), non_blocking=True),
+                   lambda: self.outs[3].copy_(s.lc["out"].index_select(0, self.g_lc), non_blocking=True),
+                   lambda: self.outs[4].copy_(s.lc["kv_cache"], non_blocking=True)]
         for i in range(5):
+            for ev in ready[i]:
+                stream.wait_event(ev)
             s.call(i)
-        self.outs[0].copy_(s.pd["kv_cache"].view(-1).index_select(0, self.g_pd), non_blocking=True)
-        self.outs[1].copy_(s.cd["out"].index_select(0, self.g_cd), non_blocking=True)
-        self.outs[2].copy_(s.cp["out"].index_select(0, self.g_cp), non_blocking=True)
-        self.outs[3].copy_(s.lc["out"].index_select(0, self.g_lc), non_blocking=True)
-        self.outs[4].copy_(s.lc["kv_cache"], non_blocking=True)
+            gathers[i]()
 
 
 # --------------------------------------------------------- CPU oracle sample
