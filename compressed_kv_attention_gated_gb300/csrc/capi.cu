@@ -65,7 +65,7 @@ const char* ckv_status_string(ckv_status s) {
     case CKV_ERR_NULL: return "a required pointer is NULL";
     case CKV_ERR_SHAPE: return "unsupported or inconsistent size, stride or flag";
     case CKV_ERR_DTYPE: return "unsupported input dtype";
-    case CKV_ERR_ALIGN: return "pointer or stride breaks the 16-byte alignment rule";
+    case CKV_ERR_ALIGN: return "pointer or stride misaligned (16 bytes for row data, element size for index arrays)";
     case CKV_ERR_PLAN: return "planner: invalid lengths, token count or capacity";
     case CKV_ERR_CUDA: return "CUDA runtime error (see ckv_last_cuda_error)";
     default: return "unknown status";
@@ -94,7 +94,8 @@ ckv_status ckv_kpool_decode_update(uint8_t* kv_cache, int64_t num_pages, int32_t
   if (!aligned(kv_cache, 16) || !aligned(tail_ring, 16) || !aligned(key, 16) ||
       !aligned(score, 16) || !aligned(ape, 16) || key_stride_b % 8 || key_stride_t % 8 ||
       score_stride_b % 8 || score_stride_t % 8 || !aligned(tap_x, 16) || !aligned(tap_xb, 8) ||
-      !aligned(tap_yb, 8))
+      !aligned(tap_yb, 8) || !aligned(tail_slot_mapping, 4) || !aligned(slot_mapping, 4) ||
+      !aligned(positions, 4) || !aligned(err_word, 4))
     return CKV_ERR_ALIGN;
   ckv::KpoolDecodeArgs a{};
   a.cache = kv_cache;
@@ -138,7 +139,8 @@ ckv_status ckv_kpool_compress(uint8_t* kv_cache, int64_t num_pages, int32_t page
   if (!slot_k || !slot_score || !ape || (write_cache && (!kv_cache || !loc))) return CKV_ERR_NULL;
   if (!aligned(slot_k, 16) || !aligned(slot_score, 16) || !aligned(ape, 16) ||
       !aligned(kv_cache, 16) || !aligned(out_fp8, 16) || !aligned(tap_x, 16) ||
-      !aligned(tap_xb, 8) || !aligned(tap_yb, 8) || !aligned(loc, 8))
+      !aligned(tap_xb, 8) || !aligned(tap_yb, 8) || !aligned(loc, 8) || !aligned(out_scale, 4) ||
+      !aligned(err_word, 4))
     return CKV_ERR_ALIGN;
   ckv::KpoolCompressArgs a{};
   a.cache = kv_cache;
@@ -168,7 +170,9 @@ ckv_status ckv_kpool_seed_tail(uint16_t* tail_ring, int64_t num_tail_blocks, con
   if (n_tokens == 0) return CKV_OK;
   if (n_tokens > (static_cast<int64_t>(INT32_MAX) / 32) * 8) return CKV_ERR_SHAPE;
   if (!tail_ring || !key || !score || !tslot) return CKV_ERR_NULL;
-  if (!aligned(tail_ring, 16) || !aligned(key, 16) || !aligned(score, 16)) return CKV_ERR_ALIGN;
+  if (!aligned(tail_ring, 16) || !aligned(key, 16) || !aligned(score, 16) || !aligned(tslot, 4) ||
+      !aligned(err_word, 4))
+    return CKV_ERR_ALIGN;
   ckv::KpoolSeedArgs a{};
   a.ring = tail_ring;
   a.num_blocks = num_tail_blocks;
@@ -189,6 +193,7 @@ ckv_status ckv_expand_pools_and_append_tail(const int32_t* pool_ids, int64_t poo
   if (rows == 0 || cols == 0) return CKV_OK;
   if (cols > static_cast<int64_t>(INT32_MAX) - 256) return CKV_ERR_SHAPE;
   if (!seq_lens || !out || (n_groups > 0 && !pool_ids)) return CKV_ERR_NULL;
+  if (!aligned(pool_ids, 4) || !aligned(seq_lens, 8) || !aligned(out, 4)) return CKV_ERR_ALIGN;
   ckv::ExpandArgs a{};
   a.pool_ids = pool_ids;
   a.stride = pool_ids_stride;
@@ -208,7 +213,8 @@ ckv_status ckv_c128_online_decode(float* state, int64_t num_slots, const void* i
   if (in_dtype != CKV_F32 && in_dtype != CKV_BF16) return CKV_ERR_DTYPE;
   if (B == 0) return CKV_OK;
   if (!state || !input || !out || !ape || !indices || !seq_lens) return CKV_ERR_NULL;
-  if (!aligned(state, 16) || !aligned(input, 16) || !aligned(out, 16) || !aligned(ape, 16))
+  if (!aligned(state, 16) || !aligned(input, 16) || !aligned(out, 16) || !aligned(ape, 16) ||
+      !aligned(indices, 4) || !aligned(seq_lens, 4) || !aligned(err_word, 4))
     return CKV_ERR_ALIGN;
   ckv::C128DecodeArgs a{};
   a.state = state;
@@ -243,7 +249,8 @@ ckv_status ckv_c128_online_prefill(float* state, int64_t num_slots, const void* 
   if (!state || !input || !ape || !indices) return CKV_ERR_NULL;
   if ((num_compress && (!compress_plan || !out)) || (num_write && !write_plan)) return CKV_ERR_NULL;
   if (!aligned(state, 16) || !aligned(input, 16) || !aligned(out, 16) || !aligned(ape, 16) ||
-      !aligned(compress_plan, 16) || !aligned(write_plan, 16))
+      !aligned(compress_plan, 16) || !aligned(write_plan, 16) || !aligned(indices, 4) ||
+      !aligned(load_indices, 4) || !aligned(err_word, 4))
     return CKV_ERR_ALIGN;
   ckv::C128PrefillArgs a{};
   a.state = state;
@@ -287,7 +294,8 @@ ckv_status ckv_c128_online_prefill_counted(float* state, int64_t num_slots, cons
   if (!state || !input || !ape || !indices || !out || !compress_plan || !write_plan || !counts)
     return CKV_ERR_NULL;
   if (!aligned(state, 16) || !aligned(input, 16) || !aligned(out, 16) || !aligned(ape, 16) ||
-      !aligned(compress_plan, 16) || !aligned(write_plan, 16) || !aligned(counts, 4))
+      !aligned(compress_plan, 16) || !aligned(write_plan, 16) || !aligned(counts, 4) ||
+      !aligned(indices, 4) || !aligned(load_indices, 4) || !aligned(err_word, 4))
     return CKV_ERR_ALIGN;
   ckv::C128PrefillArgs a{};
   a.state = state;
@@ -319,7 +327,7 @@ ckv_status ckv_plan_online_prefill_device(const int64_t* seq_lens, const int64_t
   if (B > 0 && (!seq_lens || !extend_lens)) return CKV_ERR_NULL;
   if (num_tokens > 0 && (!compress_plan || !write_plan)) return CKV_ERR_NULL;
   if (!aligned(compress_plan, 16) || !aligned(write_plan, 16) || !aligned(counts, 4) ||
-      !aligned(seq_lens, 8) || !aligned(extend_lens, 8))
+      !aligned(seq_lens, 8) || !aligned(extend_lens, 8) || !aligned(err_word, 4))
     return CKV_ERR_ALIGN;
   return cuda_status(ckv::launch_plan_device(seq_lens, extend_lens, B, num_tokens, compress_plan,
                                              write_plan, pad_for_graph != 0, counts, err_word,
@@ -344,7 +352,8 @@ ckv_status ckv_check_distinct(const void* ids, int32_t id_bytes, int64_t n, int6
     return CKV_ERR_SHAPE;
   if (scratch_words < (range + 31) / 32) return CKV_ERR_SHAPE;
   if (!scratch || !err_word || (n > 0 && !ids)) return CKV_ERR_NULL;
-  if (!aligned(ids, static_cast<uintptr_t>(id_bytes)) || !aligned(scratch, 4)) return CKV_ERR_ALIGN;
+  if (!aligned(ids, static_cast<uintptr_t>(id_bytes)) || !aligned(scratch, 4) || !aligned(err_word, 4))
+    return CKV_ERR_ALIGN;
   return cuda_status(ckv::launch_check_distinct(ids, id_bytes, n, range, scratch, err_word,
                                                 static_cast<cudaStream_t>(stream)));
 }

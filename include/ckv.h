@@ -49,7 +49,7 @@ typedef int32_t ckv_status;
 #define CKV_ERR_NULL 1       /* a required pointer is NULL */
 #define CKV_ERR_SHAPE 2      /* unsupported or inconsistent size, stride or flag */
 #define CKV_ERR_DTYPE 3      /* unsupported input dtype */
-#define CKV_ERR_ALIGN 4      /* a pointer or stride breaks the 16-byte alignment rule */
+#define CKV_ERR_ALIGN 4      /* a pointer or stride is misaligned: 16 bytes for row data, the element size for index arrays and err_word */
 #define CKV_ERR_PLAN 5       /* planner: bad lengths, token count or capacity */
 #define CKV_ERR_CUDA 6       /* a CUDA runtime call failed (see ckv_last_cuda_error) */
 

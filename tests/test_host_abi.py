@@ -74,6 +74,17 @@ def test_validation_rejects_before_launch(lib):
     assert lib.ckv_kpool_decode_update(one, 1, 16, one, 1, one, one, one, one, 512, 128, one, 512, 128, one,
                                        0, 4, 16, 128, 1, None, None, None, 0, None, None) == 0  # empty batch
     assert lib.ckv_kpool_seed_tail(one, 1, one, one, one, 5, 16, 96, None, None) == 2
+    # element alignment of the index arrays and of the error word (a misaligned
+    # typed pointer would fault on the device): rejected on the host
+    odd = P(18)
+    assert lib.ckv_c128_online_decode(one, 4, one, 0, one, one, odd, one, 3, 128, 0, None, None) == 4
+    assert lib.ckv_c128_online_decode(one, 4, one, 0, one, one, one, one, 3, 128, 0, odd, None) == 4
+    assert lib.ckv_c128_online_prefill(one, 4, one, 0, 10, one, one, odd, None, 2, one, 3, None, 0, 512, 0,
+                                       None, None) == 4
+    assert lib.ckv_kpool_seed_tail(one, 1, one, one, odd, 5, 16, 128, None, None) == 4
+    assert lib.ckv_kpool_decode_update(one, 1, 16, one, 1, odd, one, one, one, 512, 128, one, 512, 128, one,
+                                       2, 4, 16, 128, 1, None, None, None, 0, None, None) == 4
+    assert lib.ckv_expand_pools_and_append_tail(odd, 4, one, 2, 4, 16, one, 0, None) == 4
     # distinct-id check: id width, range, scratch size, required pointers, alignment
     chk = lib.ckv_check_distinct
     chk.argtypes = [P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, P, ctypes.c_int64, P, P]
