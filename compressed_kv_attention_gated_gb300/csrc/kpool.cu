@@ -197,12 +197,13 @@ __device__ __forceinline__ void cache_write(uint8_t* cache, int64_t page_size, i
   if (lane == 0) *reinterpret_cast<float*>(base + page_size * kD + 4 * tok) = scale;
 }
 
-// Wait for the preceding grid (programmatic dependent launch; a no-op
-// otherwise), then stage the [P][128] bias table in shared memory, multiplied
-// by log2(e), and let the next grid in the stream begin launching.
+// Stage the [P][128] bias table in shared memory, multiplied by log2(e), and
+// let the next grid in the stream begin launching.  The caller has waited for
+// the preceding grid (programmatic dependent launch; a no-op otherwise) and
+// has usually issued its first row loads already, so that their latency and
+// the staging overlap.
 template <int P>
 __device__ __forceinline__ void stage_ape(float* s_ape2, const float* ape) {
-  pdl_wait();
   for (int i = threadIdx.x; i < P * kD / 4; i += blockDim.x) {
     float4 v = ld_shared_ro_f4(ape + 4 * i);
     v.x *= kLog2e;
@@ -222,22 +223,25 @@ template <int P, bool kRound>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
     kpool_compress_kernel(const __grid_constant__ KpoolCompressArgs a) {
   __shared__ __align__(16) float s_ape[P * kD];
-  stage_ape<P>(s_ape, a.ape);
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t pool = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
-  if (pool >= a.n_pools) return;
-  if (a.write_mask && a.write_mask[pool] == 0) return;
-
-  // the cache location travels with the rows, not after the arithmetic
-  const int64_t loc = a.write_cache ? a.loc[pool] : 0;
+  const bool want = pool < a.n_pools && (!a.write_mask || a.write_mask[pool] != 0);
+  // the rows and the cache location are in flight while the bias is staged
+  int64_t loc = 0;
   uint2 kr[P], sr[P];
-  const uint16_t* kb = a.slot_k + pool * P * kD + 4 * lane;
-  const uint16_t* sb = a.slot_score + pool * P * kD + 4 * lane;
+  if (want) {
+    loc = a.write_cache ? a.loc[pool] : 0;
+    const uint16_t* kb = a.slot_k + pool * P * kD + 4 * lane;
+    const uint16_t* sb = a.slot_score + pool * P * kD + 4 * lane;
 #pragma unroll
-  for (int j = 0; j < P; ++j) {
-    kr[j] = ld_stream_u2(kb + j * kD);
-    sr[j] = ld_stream_u2(sb + j * kD);
+    for (int j = 0; j < P; ++j) {
+      kr[j] = ld_stream_u2(kb + j * kD);
+      sr[j] = ld_stream_u2(sb + j * kD);
+    }
   }
+  stage_ape<P>(s_ape, a.ape);
+  if (!want) return;
   float x[4], xb[4], yb[4], scale;
   uint32_t codes;
   pool_softmax<P>(kr, sr, s_ape, lane, x);
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 1)
     for (int s = 0; s < kBulkStages; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
   }
-  stage_ape<P>(s_ape, a.ape);  // ends with __syncthreads()
+  pdl_wait();
 
   const int64_t W = static_cast<int64_t>(gridDim.x) * kBulkWarps;
   const int64_t first = static_cast<int64_t>(blockIdx.x) * kBulkWarps + warp;
@@ -307,6 +311,7 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 1)
   }
   for (int s = 0; s < kBulkStages; ++s)
     if (wanted(first + s * W)) armed |= 1u << s;
+  stage_ape<P>(s_ape, a.ape);  // overlaps the first copies; ends with __syncthreads()
 
   // cache locations are fetched one pool ahead so that no global load sits
   // between a pool's arithmetic and its store
@@ -383,15 +388,15 @@ template <int P, bool kRound>
 __global__ void __launch_bounds__(kDecodeCtaWarps * 32)
     kpool_decode_kernel(const __grid_constant__ KpoolDecodeArgs a) {
   __shared__ __align__(16) float s_ape[P * kD];
-  stage_ape<P>(s_ape, a.ape);
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.x * kDecodeCtaWarps + (threadIdx.x >> 5);
-  if (b >= a.B) return;
+  const bool active = b < a.B;
   const int64_t cache_rows = a.num_pages * a.page_size;
 
-  for (int t0 = 0; t0 < a.N; t0 += kPrefetch) {
-    int32_t loc[kPrefetch], pos[kPrefetch], tslot[kPrefetch];
-    uint2 kc[kPrefetch], sc[kPrefetch];
+  int32_t loc[kPrefetch], pos[kPrefetch], tslot[kPrefetch];
+  uint2 kc[kPrefetch], sc[kPrefetch];
+  auto load_group = [&](int t0) {
 #pragma unroll
     for (int i = 0; i < kPrefetch; ++i) {
       const int t = t0 + i;
@@ -407,6 +412,13 @@ __global__ void __launch_bounds__(kDecodeCtaWarps * 32)
         kc[i] = sc[i] = make_uint2(0u, 0u);
       }
     }
+  };
+  if (active) load_group(0);  // in flight while the bias is staged
+  stage_ape<P>(s_ape, a.ape);
+  if (!active) return;
+
+  for (int t0 = 0; t0 < a.N; t0 += kPrefetch) {
+    if (t0 > 0) load_group(t0);
 #pragma unroll
     for (int i = 0; i < kPrefetch; ++i) {
       const int slot = max(pos[i], 0) & (P - 1);
