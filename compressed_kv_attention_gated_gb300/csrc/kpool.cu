@@ -537,7 +537,10 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
       if (dst[u]) *reinterpret_cast<uint2*>(dst[u]) = v[u];
   }
 }
-constexpr int64_t kBulkMinPools = 4096;
+// Automatic choice: one warp per pool below 65,536 pools, the persistent
+// bulk-copy pipeline from there (measured: warp per pool faster by 6-21% up to
+// 16,384 pools, equal at 65,536, 3% slower at 262,144).
+constexpr int64_t kBulkMinPools = 65536;
 
 template <int P, bool kRound, int W, int S>
 cudaError_t compress_bulk(const KpoolCompressArgs& a, bool use_pdl, cudaStream_t s) {

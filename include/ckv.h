@@ -272,7 +272,7 @@ int32_t ckv_c128_prefill_set_variant(int32_t variant);
 /*
  * Kernel choice for ckv_kpool_compress (process-wide).
  *   0 = automatic (default): the persistent bulk-copy pipeline for at least
- *       4096 pools, otherwise one warp per pool;
+ *       65536 pools, otherwise one warp per pool;
  *   1 = always one warp per pool;  2 = always the bulk-copy pipeline.
  * Both compute the same function.  Returns the previous setting, or -1 (and
  * changes nothing) for an unknown value.
