@@ -274,7 +274,12 @@ cudaError_t decode_d(const C128DecodeArgs& a, bool use_pdl, cudaStream_t s) {
                    a);
 }
 
-constexpr uint32_t kTmaMinSegments = 32;
+// Automatic choice: the persistent TMA pipeline from 1024 compress segments
+// (measured, one request from position 0: the one-CTA-per-segment kernel is
+// faster up to 512 segments -- its CTAs need no bias staging or pipeline fill
+// -- the two are equal for fp32 at 2048 and the pipeline is 7% faster for
+// bf16 at 2048 and 13% at 8192).
+constexpr uint32_t kTmaMinSegments = 1024;
 
 template <int D, typename InT>
 cudaError_t prefill_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
@@ -283,8 +288,6 @@ cudaError_t prefill_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
   if (a.num_compress) {
     const int v = prefill_variant();
     cudaError_t e = cudaErrorNotSupported;
-    // Automatic choice: the TMA pipeline when there are enough segments to
-    // amortise its per-CTA set-up (bias staging, pipeline fill).
     const bool tma = v == 2 || (v == 0 && a.num_compress >= kTmaMinSegments);
     if (tma && c128_prefill_tma_supported(a, D, dtype)) {
       e = launch_c128_prefill_compress_tma(a, D, dtype, use_pdl, s);

@@ -260,7 +260,7 @@ ckv_status ckv_c128_online_prefill(float* state, int64_t num_slots, const void* 
 /*
  * Kernel choice for the compress pass of ckv_c128_online_prefill (process-wide).
  *   0 = automatic (default): the TMA-pipelined persistent kernel when there
- *       are at least 32 compress segments, otherwise the one-CTA-per-segment
+ *       are at least 1024 compress segments, otherwise the one-CTA-per-segment
  *       kernel;
  *   1 = always the one-CTA-per-segment kernel;
  *   2 = always the TMA-pipelined kernel (when the device supports it).
