@@ -171,23 +171,14 @@ __global__ void __launch_bounds__(Layout<InT>::kThreads, 1)
     mbar_init(&ready[1], kCWarps);
     fence_mbar_init();
   }
+  __syncthreads();  // barriers initialised before anyone waits on them
   pdl_wait();
   const uint32_t n = a.counts ? min(a.counts[0], a.num_compress) : a.num_compress;
-  // bias slice, pre-scaled to the log2 domain
-  for (int i = threadIdx.x; i < 128 * kCh / 4; i += kThreads) {
-    const int j = i / (kCh / 4), c4 = i % (kCh / 4);
-    float4 v = ld_shared_ro_f4(a.ape + j * D + slice * kCh + 4 * c4);
-    v.x *= kLog2e;
-    v.y *= kLog2e;
-    v.z *= kLog2e;
-    v.w *= kLog2e;
-    reinterpret_cast<float4*>(s_ape)[i] = v;
-  }
-  __syncthreads();
-  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // starts streaming at once: only the consumers need the bias slice
+    pdl_trigger();
     if (lane != 0) return;
     uint32_t st = 0, ph = 0, armed = 0;
     bool aborted = false;
@@ -223,6 +214,19 @@ __global__ void __launch_bounds__(Layout<InT>::kThreads, 1)
   }
 
   // -------------------------------------------------------------- consumers
+  // bias slice, pre-scaled to the log2 domain, staged by the consumer warps
+  // (named barrier 1) while the producer's first loads are in flight
+  for (int i = threadIdx.x - 32; i < 128 * kCh / 4; i += kThreads - 32) {
+    const int j = i / (kCh / 4), c4 = i % (kCh / 4);
+    float4 v = ld_shared_ro_f4(a.ape + j * D + slice * kCh + 4 * c4);
+    v.x *= kLog2e;
+    v.y *= kLog2e;
+    v.z *= kLog2e;
+    v.w *= kLog2e;
+    reinterpret_cast<float4*>(s_ape)[i] = v;
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(kCWarps * 32) : "memory");
+  pdl_trigger();
   const int cw = warp - 1;
   const int t = cw * 32 + lane;  // channel of the slice in the epilogue (t < kCh)
   uint32_t st = 0, ph = 0, it = 0;
