@@ -42,41 +42,43 @@ constexpr int kDecodeMinBlocks = 4;  // CTAs per SM (64 registers, no spills)
 template <int D, typename InT, int G, int kMinBlocks>
 __global__ void __launch_bounds__(kDecodeThreads, kMinBlocks)
     c128_decode_kernel(const __grid_constant__ C128DecodeArgs a) {
-  constexpr int kTpr = D / (4 * G);             // threads per request
+  constexpr int kTpr = D / (4 * G);             // threads per request (even)
   constexpr int kRpc = kDecodeThreads / kTpr;   // requests per CTA
   constexpr int kSpan = D / G;                  // channel distance between groups
   pdl_wait();
   pdl_trigger();
   const int t = threadIdx.x % kTpr;
   const int b = blockIdx.x * kRpc + threadIdx.x / kTpr;
-  if (b >= a.B) return;
+  // no early return: lane pairs exchange a flag at the end
+  const bool in_batch = b < a.B;
 
   // The slot index gates the dependent state loads: issue it before the input stream.
-  const int32_t index = a.indices[b];
-  const int32_t seq_len = a.seq_lens[b];
+  const int32_t index = in_batch ? a.indices[b] : 0;
+  const int32_t seq_len = in_batch ? a.seq_lens[b] : 1;
   const int col = 4 * t;
-  const InT* in = static_cast<const InT*>(a.input) + static_cast<int64_t>(b) * 2 * D;
+  const InT* in = static_cast<const InT*>(a.input) + static_cast<int64_t>(in_batch ? b : 0) * 2 * D;
   float4 kin[G], sin_[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     kin[g] = In4<InT>::load(in, col + kSpan * g);
     sin_[g] = In4<InT>::load(in + D, col + kSpan * g);
   }
-  if (seq_len < 1) {
+  bool ok = in_batch;
+  if (ok && seq_len < 1) {
     if (t == 0) flag_error(a.err, CKV_DEVERR_SEQ_LEN);
-    return;
+    ok = false;
   }
-  if (index < 0 || index >= a.num_slots) {
+  if (ok && (index < 0 || index >= a.num_slots)) {
     if (t == 0) flag_error(a.err, CKV_DEVERR_SLOT);
-    return;
+    ok = false;
   }
-  const int p = (seq_len - 1) & 127;  // chunk position of the new token
-  float* st = a.state + static_cast<int64_t>(index) * 3 * D + col;
+  const int p = ok ? (seq_len - 1) & 127 : 0;  // chunk position of the new token
+  float* st = a.state + static_cast<int64_t>(ok ? index : 0) * 3 * D + col;
 
   float4 ap[G], om[G], os[G], okv[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) ap[g] = ld_shared_ro_f4(a.ape + p * D + col + kSpan * g);
-  if (p != 0) {
+  if (ok && p != 0) {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       om[g] = *reinterpret_cast<const float4*>(st + kSpan * g);
@@ -85,8 +87,10 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinBlocks)
     }
   }
   float4 nm[G], ns[G], nkv[G];
+  bool max_same[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
+    max_same[g] = ok && p != 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float z = get(sin_[g], i) + get(ap[g], i);
@@ -104,9 +108,14 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinBlocks)
         set(nm[g], i, M);
         set(ns[g], i, s);
         set(nkv[g], i, (get(okv[g], i) * w1 + k * w2) / s);
+        max_same[g] = max_same[g] && __float_as_uint(M) == __float_as_uint(m1);
       }
     }
+    // the 32-byte sector of the max row shared with the partner lane is left
+    // as it is (the new bits equal the stored ones) when neither half changed
+    max_same[g] = __shfl_xor_sync(0xFFFFFFFFu, max_same[g], 1) && max_same[g];
   }
+  if (!ok) return;
   if (p == 127) {
     float* o = a.out + static_cast<int64_t>(b) * D + col;
 #pragma unroll
@@ -114,7 +123,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinBlocks)
   } else {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      *reinterpret_cast<float4*>(st + kSpan * g) = nm[g];
+      if (!max_same[g]) *reinterpret_cast<float4*>(st + kSpan * g) = nm[g];
       *reinterpret_cast<float4*>(st + D + kSpan * g) = ns[g];
       *reinterpret_cast<float4*>(st + 2 * D + kSpan * g) = nkv[g];
     }
