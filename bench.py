@@ -695,6 +695,11 @@ def run_case(args):
 
 
 def run_rotation(args):
+    """--case c128_decode|kpool_decode --rotate: print rotation_timings() as one JSON line."""
+    print(json.dumps(rotation_timings(args.case, args.steps, args.warmup)))
+
+
+def rotation_timings(case, replays=100, warmup=20):
     """Decode calls timed L2-cold and warm, each replayed from one CUDA graph.
 
     Cold: R independent instances of the batch (R x algorithmic bytes >= 4 x
@@ -714,7 +719,7 @@ def run_rotation(args):
     torch.cuda.set_device(dev)
     err = torch.zeros((1,), dtype=torch.int32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    if args.case == "c128_decode":
+    if case == "c128_decode":
         first = synth.c128_decode(dev, seed=100)
         nbytes = c128_decode_bytes(first)[0]
 
@@ -724,7 +729,7 @@ def run_rotation(args):
         def call(d, pdl):
             ck.ckv_c128_online_decode(d["state"], d["input"], d["out"], d["ape"], d["indices"], d["seq_lens"],
                                       use_pdl=pdl, err_word=err)
-    elif args.case == "kpool_decode":
+    elif case == "kpool_decode":
         first = synth.pooled_decode(dev, seed=100)
         nbytes = kpool_decode_bytes(first)[0]
         B, ps = first["B"], first["page_size"]
@@ -749,16 +754,16 @@ def run_rotation(args):
     inst = [make(r) for r in range(R)]
     peak, peak_kind = _peaks()
     stream = torch.cuda.Stream(dev)
-    res = {"case": args.case, "mode": "rotate", "instances": R, "l2_bytes": l2, "bytes_per_call": nbytes,
-           "replays": args.steps}
+    res = {"case": case, "mode": "rotate", "instances": R, "l2_bytes": l2, "bytes_per_call": nbytes,
+           "replays": replays}
 
     def timed(graph, n_calls):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t = []
         with torch.cuda.stream(stream):
-            for _ in range(max(20, args.warmup)):
+            for _ in range(max(20, warmup)):
                 graph.replay()
-            for _ in range(args.steps):
+            for _ in range(replays):
                 e0.record(stream)
                 graph.replay()
                 e1.record(stream)
@@ -788,7 +793,9 @@ def run_rotation(args):
     torch.cuda.synchronize()
     res["err"] = int(err.item())
     res["peak_gbs"] = peak
-    print(json.dumps(res))
+    del inst
+    torch.cuda.empty_cache()
+    return res
 
 
 def main():
@@ -807,6 +814,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode-cold", action="store_true",
+                    help="skip the L2-cold CUDA-graph timing of the two decode calls")
     ap.add_argument("--no-pdl", action="store_true", help="plain stream order between the five calls")
     ap.add_argument("--no-overlap", action="store_true", help="run the decode calls on the prefill stream")
     ap.add_argument("--copy-streams", type=int, default=4, help="streams sharing the large H2D copies (e2e)")
@@ -957,6 +966,18 @@ def main():
         cpu["single_thread"] = {"value": tokens_step / cpu_step_estimate(res1, step.tokens), "cores": 1,
                                 "sample": sample1}
 
+    decode_cold = None
+    if rank == 0 and ws == 1 and not args.no_decode_cold:  # rotating instances on the one GPU
+        decode_cold = {}
+        for name, case in (("kpool_decode_update", "kpool_decode"), ("c128_online_decode", "c128_decode")):
+            r = rotation_timings(case)
+            decode_cold[name] = {"instances": r["instances"], "bytes_per_call": r["bytes_per_call"],
+                                 "us_per_call_cold": r["pdl"]["us_per_call_cold"], "gbs_cold": r["pdl"]["gbs_cold"],
+                                 "frac": r["pdl"][f"frac_of_{peak_kind}_hbm"],
+                                 "us_single_call_warm": r["pdl"]["us_single_call_warm"], "err": r["err"]}
+        decode_cold["method"] = ("R instances (R x bytes per call >= 4 x L2), one call on each, captured in order "
+                                 "in one CUDA graph with programmatic dependent launch; median of 100 replays / R")
+
     if rank == 0:
         print(json.dumps({
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": warmup,
@@ -969,7 +990,7 @@ def main():
                                ("; decode calls on a second stream, concurrent with the prefill calls"
                                 if overlap else "; one stream"),
             "breakdown_ms_per_step": round(breakdown_ms, 4), "kernels": kernels, "roofline": roofline, "clocks": clk.summary(),
-            "gpu_launches": step.launches() * K, "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": step.launches() * K, "e2e": e2e, "cpu_baseline": cpu, "decode_l2_cold": decode_cold,
         }), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
