@@ -237,8 +237,11 @@ ckv_status ckv_c128_online_decode(float* state, int64_t num_slots, const void* i
  *      out[ragged_id].  The state buffer is only read.
  *   2. write pass over write_plan[0..num_write): the same reduction, whose
  *      (max, sum, kv) is stored into slot indices[batch_id].
- * The second launch starts after every read of the first has completed, so
- * a slot read in pass 1 may be overwritten in pass 2.
+ * The second pass touches the state only after the first pass has completed,
+ * so a slot read in pass 1 may be overwritten in pass 2.  With use_pdl the
+ * second pass may start reading its plan, indices and input tokens while the
+ * first pass still runs (nothing it reads except the state is written by the
+ * first pass); without it the two launches are plainly stream ordered.
  * state          device fp32 [num_slots][3][D].
  * input          device [num_tokens][2D] (kv | score), fp32 or bf16.
  * out            device fp32 [num_tokens][D]; only compress rows are written.
