@@ -82,6 +82,7 @@ def lib():
                                             P(i64), ci, ci, P(f64), P(u8), P(f64), P(i32), ci]),
                 "ora_plan_segments": (ci, [P(i64), P(i64), ci, P(u32), P(u32), i64, P(i64), P(i64)]),
                 "ora_expand_pools_and_append_tail": (None, [P(i32), i64, P(i64), ci, ci, ci, P(i32)]),
+                "ora_c128_rows_to_cache": (None, [P(u8), i64, P(f32), P(i64), i64, ci, ci]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -347,3 +348,16 @@ def plan_segments(seq_lens, extend_lens, cap=None):
     if rc != 0:
         raise ValueError("plan capacity exceeded")
     return c[: nc.value].copy(), w[: nw.value].copy()
+
+
+def c128_rows_to_cache(cache, page_size, rows, locs, round_scale=True):
+    """Store fp32 rows [n, D] into the paged FP8 cache (uint8 [pages, page_size,
+    D + 4*D/128], updated in place), 128-channel block by block through the
+    pooled output stage; rows with a negative location are skipped."""
+    rows = np.ascontiguousarray(rows, dtype=np.float32)
+    locs = np.ascontiguousarray(locs, dtype=np.int64)
+    n, D = rows.shape
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous and cache.shape[2] == D + 4 * (D // 128)
+    lib().ora_c128_rows_to_cache(_p(cache, ctypes.c_uint8), int(page_size), _p(rows, ctypes.c_float),
+                                 _p(locs, ctypes.c_int64), n, D, int(bool(round_scale)))
+    return cache

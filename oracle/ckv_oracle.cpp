@@ -311,6 +311,37 @@ void ora_kpool_compress(uint8_t* cache, int64_t num_pages, int64_t page_size,
   });
 }
 
+// ---------------- c128 rows through the pooled output stage ----------------
+// [C128] compressed rows combined with the [KPOOL] output stage (neither page
+// shows the combination; reading): each 128-channel block of an fp32 row is
+// one pooled vector -- bf16 (round to nearest even), the Hadamard-128 reading
+// above, bf16, absmax FP8 with its own scale -- and the cache generalises the
+// pooled layout: per page, page_size rows of D code bytes (block j at bytes
+// 128j..), then page_size * (D/128) fp32 scales (row r, block j at r*(D/128)+j).
+// Rows with a negative location are skipped.
+void ora_c128_rows_to_cache(uint8_t* cache, int64_t page_size, const float* rows, const int64_t* locs,
+                            int64_t n, int D, int round_scale) {
+  const int blocks = D / 128;
+  const int64_t page_bytes = page_size * (D + 4 * blocks);
+  for (int64_t r = 0; r < n; ++r) {
+    if (locs[r] < 0) continue;
+    const int64_t page = locs[r] / page_size, tok = locs[r] % page_size;
+    uint8_t* base = cache + page * page_bytes;
+    for (int j = 0; j < blocks; ++j) {
+      float xf[128], yf[128];
+      uint16_t yb[128];
+      uint8_t q[128];
+      float scale;
+      for (int d = 0; d < 128; ++d) xf[d] = bf16_to_float(bf16_from_double(rows[r * D + 128 * j + d]));
+      hadamard128_fp32(xf, yf);
+      for (int d = 0; d < 128; ++d) yb[d] = bf16_from_double(yf[d]);
+      quantize_row(yb, 128, round_scale, q, &scale);
+      std::memcpy(base + tok * D + 128 * j, q, 128);
+      std::memcpy(base + page_size * D + 4 * (tok * blocks + j), &scale, 4);
+    }
+  }
+}
+
 // ------------------- pooled decode / verify update ------------------------
 // [KPOOL] _kpool_decode_update_batched_kernel, written as the ordered
 // per-request loop it describes.  Per request b and token t in order:

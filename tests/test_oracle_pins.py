@@ -601,3 +601,66 @@ def test_expand_invariants(ora):
             # the tail is exactly the tokens after the last full pool, in order, then -1s
             assert real.tolist() == list(range((seq[r] // P) * P, seq[r]))
             assert np.all(tail[len(real):] == -1)
+
+
+# ------------------------------------------- c128 rows -> paged FP8 cache
+def _bf16(x):
+    return torch.tensor(np.asarray(x, np.float32)).to(torch.bfloat16).float().numpy()
+
+
+def _e4m3(x):
+    return torch.tensor(np.asarray(x, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("round_scale", [False, True])
+def test_c128_rows_to_cache_golden(ora, round_scale):
+    """Block j of the row is (j+1)·e_0: its rotation is the constant (j+1)/sqrt(128)
+    in every channel, so every code of the block is one value and the block's
+    scale follows from that constant alone.  Row at location 5 of a
+    4-row-per-page cache: page 1, row 1; scales of row 1 at footer 4..7."""
+    D, ps = 512, 4
+    cache = np.zeros((2, ps, D + 16), np.uint8)
+    row = np.zeros((1, D), np.float32)
+    for j in range(4):
+        row[0, 128 * j] = j + 1
+    ora.c128_rows_to_cache(cache, ps, row, np.array([5]), round_scale=round_scale)
+    c = np.float32(1.0 / np.sqrt(128.0))
+    expect = cache.copy() * 0
+    for j in range(4):
+        y = _bf16(np.float32(j + 1) * c)  # the fp32 butterfly of e_0 is exact; one multiply, then bf16
+        v = np.float32(y * np.float32(1.0 / 448.0))
+        scale = np.float32(2.0 ** np.ceil(np.log2(np.float64(v)))) if round_scale else v
+        q = _e4m3(np.clip(np.float32(y / scale), -448, 448))
+        page = expect[1].reshape(-1)  # a page: 4 rows of D code bytes, then 4 x 4 fp32 scales
+        page[1 * D + 128 * j:1 * D + 128 * j + 128] = q
+        page[ps * D + 4 * (4 * 1 + j):ps * D + 4 * (4 * 1 + j) + 4] = np.array([scale], np.float32).view(np.uint8)
+    np.testing.assert_array_equal(cache, expect)
+    if not round_scale:
+        assert np.all(cache[1].reshape(-1)[D:2 * D] == 0x7E)  # 448, the largest e4m3 value
+
+
+@pytest.mark.parametrize("round_scale", [False, True])
+def test_c128_rows_to_cache_inverse_rotation(ora, round_scale):
+    """Decoding the codes, scaling them and applying the inverse of the
+    orthonormal Hadamard matrix (itself) recovers each 128-block of the row to
+    FP8 precision; a wrong rotation order, block offset or scale index would not."""
+    from scipy.linalg import hadamard
+
+    rng = np.random.default_rng(7)
+    D, ps, n = 256, 8, 10
+    rows = (rng.standard_normal((n, D)) * np.repeat(rng.uniform(0.01, 30, (n, D // 128)), 128, axis=1))
+    rows = rows.astype(np.float32)
+    locs = rng.permutation(3 * ps)[:n].astype(np.int64)
+    cache = np.zeros((3, ps, D + 8), np.uint8)
+    ora.c128_rows_to_cache(cache, ps, rows, locs, round_scale=round_scale)
+    H = hadamard(128) / np.sqrt(128.0)
+    flat = cache.reshape(3, -1)
+    for r in range(n):
+        page, tok = divmod(int(locs[r]), ps)
+        codes = flat[page, tok * D:tok * D + D]
+        deq = torch.tensor(codes).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+        scales = flat[page, ps * D + 4 * tok * 2: ps * D + 4 * tok * 2 + 8].view(np.float32)
+        for j in range(2):
+            x = rows[r, 128 * j:128 * j + 128].astype(np.float64)
+            back = H @ (deq[128 * j:128 * j + 128] * scales[j])
+            assert np.linalg.norm(back - x) <= 0.08 * np.linalg.norm(x), (r, j)
