@@ -612,6 +612,33 @@ def run_case(args):
             ck.ckv_c128_online_prefill(d["state"], d["input"], d["out"], d["ape"], d["indices"], c, nc, w, nw,
                                        err_word=err)
         nbytes = n * 2 * 512 * d["input"].element_size() + nc * 2048
+    elif args.case in ("prefill_bf16_fp8", "prefill_f32_fp8"):
+        # the c128 prefill with the FP8 output stage only (no fp32 rows)
+        bf = args.case == "prefill_bf16_fp8"
+        d = synth.c128_prefill(dev, seed=5, B=1, D=512, max_extend=n, zero_prefix=True, num_slots=1,
+                               dtype=torch.bfloat16 if bf else torch.float32,
+                               score_dist="student_t" if bf else "normal")
+        cpl, wpl, nc, nw = ck.ckv_plan_online_prefill(d["seq_lens"], d["extend_lens"])
+        c, w = cpl[:max(nc, 1)].to(dev), wpl[:max(nw, 1)].to(dev)
+        ps = 64
+        cache = torch.zeros(((nc + ps - 1) // ps + 1, ps, 512 + 16), device=dev, dtype=torch.uint8)
+        cache_loc = torch.full((n,), -1, device=dev, dtype=torch.int64)
+        cache_loc[127::128] = torch.arange(nc, device=dev)
+
+        def call():
+            ck.ckv_c128_online_prefill_fp8(d["state"], d["input"], None, d["ape"], d["indices"], c, nc, w, nw, cache,
+                                           cache_loc, err_word=err)
+        nbytes = n * 2 * 512 * d["input"].element_size() + nc * (512 + 16 + 8 + 16)
+    elif args.case == "c128_decode_fp8":
+        d = synth.c128_decode(dev, seed=5)
+        ps = 64
+        cache = torch.zeros((2048 // ps + 1, ps, 512 + 16), device=dev, dtype=torch.uint8)
+        cache_loc = torch.arange(2048, device=dev, dtype=torch.int64)
+
+        def call():
+            ck.ckv_c128_online_decode_fp8(d["state"], d["input"], None, d["ape"], d["indices"], d["seq_lens"], cache,
+                                          cache_loc, err_word=err)
+        nbytes = 2048 * (4096 + 2 * 6144)
     elif args.case == "kpool_compress":
         d = synth.long_context(dev, seed=5, B=1, T=n)
 
@@ -801,8 +828,8 @@ def rotation_timings(case, replays=100, warmup=20):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
-                    help="profile one kernel alone: prefill_f32|prefill_bf16|kpool_compress|c128_decode|"
-                         "kpool_decode|seed_tail|expand|plan_device")
+                    help="profile one kernel alone: prefill_f32|prefill_bf16|prefill_f32_fp8|prefill_bf16_fp8|"
+                         "kpool_compress|c128_decode|c128_decode_fp8|kpool_decode|seed_tail|expand|plan_device")
     ap.add_argument("--case-tokens", type=int, default=131072)
     ap.add_argument("--rotate", action="store_true",
                     help="with --case c128_decode|kpool_decode: L2-cold and warm per-call time from CUDA graph "

@@ -7,7 +7,9 @@ inputs of the workloads the library is measured on.
 from .ckv import (  # noqa: F401
     CkvError,
     ckv_c128_online_decode,
+    ckv_c128_online_decode_fp8,
     ckv_c128_online_prefill,
+    ckv_c128_online_prefill_fp8,
     ckv_c128_online_prefill_counted,
     ckv_c128_prefill_set_variant,
     ckv_check_distinct,

@@ -30,6 +30,8 @@ _STATUS_FUNCS = {
     "ckv_kpool_seed_tail": 10,
     "ckv_c128_online_decode": 13,
     "ckv_c128_online_prefill": 18,
+    "ckv_c128_online_decode_fp8": 18,
+    "ckv_c128_online_prefill_fp8": 23,
     "ckv_plan_online_prefill": 9,
     "ckv_plan_online_prefill_device": 11,
     "ckv_c128_online_prefill_counted": 17,
@@ -92,6 +94,17 @@ def load():
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                 ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int32,
+                ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+            L.ckv_c128_online_decode_fp8.argtypes = [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
+                ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+            L.ckv_c128_online_prefill_fp8.argtypes = [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int32,
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
                 ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
             L.ckv_plan_online_prefill.argtypes = [
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_void_p,
@@ -336,6 +349,72 @@ def ckv_c128_online_prefill(state, input, out, ape, indices, compress_plan, num_
         _ptr(state), state.numel() // (3 * D), _ptr(input), _dtype(input), T, _ptr(out), _ptr(ape),
         _ptr(indices), _ptr(load_indices), B, _ptr(compress_plan), int(num_compress), _ptr(write_plan),
         int(num_write), D, int(bool(use_pdl)), _ptr(err_word), _stream(stream, input)))
+
+
+def _fp8_cache(kv_cache, cache_loc, D, n_loc):
+    blocks = D // 128
+    _need(kv_cache.dtype == torch.uint8 and kv_cache.is_contiguous() and kv_cache.dim() == 3
+          and kv_cache.shape[2] == D + 4 * blocks, "kv_cache must be contiguous uint8 [pages, page_size, D + 4*D/128]")
+    _need(cache_loc.dtype == torch.int64 and cache_loc.is_contiguous() and cache_loc.numel() == n_loc,
+          "cache_loc must be contiguous int64")
+    return kv_cache.shape[0], kv_cache.shape[1]
+
+
+def ckv_c128_online_decode_fp8(state, input, out, ape, indices, seq_lens, kv_cache, cache_loc, round_scale=True,
+                               use_pdl=False, err_word=None, stream=None):
+    """Online c128 decode with the FP8 output stage; see ckv_c128_online_decode_fp8
+    in include/ckv.h.  kv_cache uint8 [pages, page_size, D + 4*D/128];
+    cache_loc int64 [B]; out float32 [B, D] or None."""
+    L = load()
+    _cuda("ckv_c128_online_decode_fp8", state, input, out, ape, indices, seq_lens, kv_cache, cache_loc, err_word)
+    B = input.shape[0]
+    D = input.shape[1] // 2
+    _need(state.dtype == torch.float32 and state.is_contiguous() and state.numel() % (3 * D) == 0,
+          "state must be contiguous float32 [slots, 3, D]")
+    _need(input.is_contiguous() and input.dim() == 2, "input must be contiguous [B, 2D]")
+    _need(out is None or (out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (B, D)),
+          "out must be float32 [B, D] or None")
+    _need(ape.dtype == torch.float32 and ape.is_contiguous() and tuple(ape.shape) == (128, D), "ape must be float32 [128, D]")
+    for t in (indices, seq_lens):
+        _need(t.dtype == torch.int32 and t.is_contiguous() and t.numel() == B, "indices/seq_lens must be int32 [B]")
+    pages, ps = _fp8_cache(kv_cache, cache_loc, D, B)
+    _check("ckv_c128_online_decode_fp8", L.ckv_c128_online_decode_fp8(
+        _ptr(state), state.numel() // (3 * D), _ptr(input), _dtype(input), _ptr(out), _ptr(ape),
+        _ptr(indices), _ptr(seq_lens), B, D, _ptr(kv_cache), pages, ps, _ptr(cache_loc), int(bool(round_scale)),
+        int(bool(use_pdl)), _ptr(err_word), _stream(stream, input)))
+
+
+def ckv_c128_online_prefill_fp8(state, input, out, ape, indices, compress_plan, num_compress, write_plan,
+                                num_write, kv_cache, cache_loc, round_scale=True, load_indices=None, use_pdl=False,
+                                err_word=None, stream=None):
+    """Online c128 prefill with the FP8 output stage; see ckv_c128_online_prefill_fp8
+    in include/ckv.h.  kv_cache uint8 [pages, page_size, D + 4*D/128];
+    cache_loc int64 [T] (read at compress rows); out float32 [T, D] or None."""
+    L = load()
+    _cuda("ckv_c128_online_prefill_fp8", state, input, out, ape, indices, load_indices, compress_plan,
+          write_plan, kv_cache, cache_loc, err_word)
+    T = input.shape[0]
+    D = input.shape[1] // 2
+    B = indices.numel()
+    _need(state.dtype == torch.float32 and state.is_contiguous() and state.numel() % (3 * D) == 0,
+          "state must be contiguous float32 [slots, 3, D]")
+    _need(input.is_contiguous() and input.dim() == 2, "input must be contiguous [T, 2D]")
+    _need(out is None or (out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (T, D)),
+          "out must be float32 [T, D] or None")
+    _need(ape.dtype == torch.float32 and ape.is_contiguous() and tuple(ape.shape) == (128, D), "ape must be float32 [128, D]")
+    _need(indices.dtype == torch.int32 and indices.is_contiguous(), "indices must be int32 [B]")
+    if load_indices is not None:
+        _need(load_indices.dtype == torch.int32 and load_indices.is_contiguous() and load_indices.numel() == B,
+              "load_indices must be int32 [B]")
+    for pl, cnt in ((compress_plan, num_compress), (write_plan, num_write)):
+        _need(pl.is_contiguous() and pl.numel() * pl.element_size() >= cnt * PLAN_ENTRY_BYTES,
+              "plan tensors must hold num_* 16-byte entries")
+    pages, ps = _fp8_cache(kv_cache, cache_loc, D, T)
+    _check("ckv_c128_online_prefill_fp8", L.ckv_c128_online_prefill_fp8(
+        _ptr(state), state.numel() // (3 * D), _ptr(input), _dtype(input), T, _ptr(out), _ptr(ape),
+        _ptr(indices), _ptr(load_indices), B, _ptr(compress_plan), int(num_compress), _ptr(write_plan),
+        int(num_write), D, _ptr(kv_cache), pages, ps, _ptr(cache_loc), int(bool(round_scale)), int(bool(use_pdl)),
+        _ptr(err_word), _stream(stream, input)))
 
 
 def ckv_c128_prefill_set_variant(variant: int) -> int:

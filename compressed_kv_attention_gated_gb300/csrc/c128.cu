@@ -22,6 +22,7 @@
 #include <type_traits>
 
 #include "ckv_device.cuh"
+#include "ckv_fp8.cuh"
 #include "ckv_launch.h"
 #include "ckv_launch_util.cuh"
 
@@ -34,12 +35,16 @@ namespace {
 constexpr int kDecodeThreads = 256;
 constexpr int kDecodeGroups = 2;     // float4 channel groups per thread
 constexpr int kDecodeMinBlocks = 4;  // CTAs per SM (64 registers, no spills)
+constexpr int kDecodeFp8MinBlocks = 4;  // with the FP8 output stage
 
 // Thread t of a request owns G groups of 4 channels, 4t + (D / G) g: D / (4G)
 // threads per request and 256 / (D / (4G)) requests per CTA, so the whole
 // decode batch is resident at once and every request's loads are in flight
 // together.
-template <int D, typename InT, int G, int kMinBlocks>
+// Row marker of the FP8 output stage: this request emits no row.
+constexpr int64_t kNoRow = INT64_MIN;
+
+template <int D, typename InT, int G, int kMinBlocks, bool kFp8>
 __global__ void __launch_bounds__(kDecodeThreads, kMinBlocks)
     c128_decode_kernel(const __grid_constant__ C128DecodeArgs a) {
   constexpr int kTpr = D / (4 * G);             // threads per request (even)
@@ -115,17 +120,47 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinBlocks)
     // as it is (the new bits equal the stored ones) when neither half changed
     max_same[g] = __shfl_xor_sync(0xFFFFFFFFu, max_same[g], 1) && max_same[g];
   }
-  if (!ok) return;
-  if (p == 127) {
-    float* o = a.out + static_cast<int64_t>(b) * D + col;
+  // plain stores first, so that their registers are free for the FP8 stage
+  constexpr int kBlocks = D / 128;
+  if (ok) {
+    if (p == 127) {
+      if (a.out) {
+        float* o = a.out + static_cast<int64_t>(b) * D + col;
 #pragma unroll
-    for (int g = 0; g < G; ++g) *reinterpret_cast<float4*>(o + kSpan * g) = nkv[g];
-  } else {
+        for (int g = 0; g < G; ++g) *reinterpret_cast<float4*>(o + kSpan * g) = nkv[g];
+      }
+    } else {
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      if (!max_same[g]) *reinterpret_cast<float4*>(st + kSpan * g) = nm[g];
-      *reinterpret_cast<float4*>(st + D + kSpan * g) = ns[g];
-      *reinterpret_cast<float4*>(st + 2 * D + kSpan * g) = nkv[g];
+      for (int g = 0; g < G; ++g) {
+        if (!max_same[g]) *reinterpret_cast<float4*>(st + kSpan * g) = nm[g];
+        *reinterpret_cast<float4*>(st + D + kSpan * g) = ns[g];
+        *reinterpret_cast<float4*>(st + 2 * D + kSpan * g) = nkv[g];
+      }
+    }
+  }
+  if constexpr (kFp8) {
+    // closing rows staged per CTA, then one warp per 128-channel block
+    __shared__ __align__(16) float s_row[kRpc][D];
+    __shared__ int64_t s_loc[kRpc];
+    const int r = threadIdx.x / kTpr;
+    const bool closing = ok && p == 127;
+    if (closing) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) *reinterpret_cast<float4*>(&s_row[r][col + kSpan * g]) = nkv[g];
+    }
+    if (t == 0) s_loc[r] = closing ? a.cache_loc[b] : kNoRow;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t rows = a.num_pages * a.page_size;
+    for (int blk = warp; blk < kRpc * kBlocks; blk += kDecodeThreads / 32) {
+      const int rr = blk / kBlocks, j = blk % kBlocks;
+      const int64_t loc = s_loc[rr];
+      if (loc == kNoRow) continue;
+      if (loc < 0 || loc >= rows) {
+        if (lane == 0 && j == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
+        continue;
+      }
+      fp8_block_store(&s_row[rr][128 * j], a.cache, a.page_size, loc, kBlocks, j, lane, a.round_scale != 0);
     }
   }
 }
@@ -137,9 +172,10 @@ constexpr int kPrefillWarps = 8;                 // warps per CTA
 constexpr int kPosPerWarp = 128 / kPrefillWarps; // chunk positions per warp
 constexpr int kBatch = 8;                        // tokens loaded per round
 
-template <int D, typename InT, bool kWrite>
+template <int D, typename InT, bool kWrite, bool kFp8>
 __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
     c128_prefill_kernel(const __grid_constant__ C128PrefillArgs a) {
+  static_assert(!(kWrite && kFp8), "the FP8 output stage belongs to the compress pass");
   constexpr int S = D / 128;  // 128-channel slices per row
   __shared__ __align__(16) float4 s_m[kPrefillWarps][32];
   __shared__ __align__(16) float4 s_s[kPrefillWarps][32];
@@ -271,7 +307,21 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
     stp[D] = ssum;
     stp[2 * D] = kv;
   } else {
-    a.out[static_cast<int64_t>(ragged_id) * D + ch] = kv;
+    if (a.out) a.out[static_cast<int64_t>(ragged_id) * D + ch] = kv;
+    if constexpr (kFp8) {
+      // the slice is block `slice` of the row: staged, then warp 0 stores it
+      __shared__ __align__(16) float s_row[128];
+      s_row[t] = kv;
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // the 128 epilogue threads
+      if (t < 32) {
+        const int64_t loc = a.cache_loc[ragged_id];
+        if (loc < 0 || loc >= a.num_pages * a.page_size) {
+          if (t == 0 && slice == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
+        } else {
+          fp8_block_store(s_row, a.cache, a.page_size, loc, S, slice, t, a.round_scale != 0);
+        }
+      }
+    }
   }
 }
 
@@ -279,7 +329,10 @@ template <int D, typename InT>
 cudaError_t decode_d(const C128DecodeArgs& a, bool use_pdl, cudaStream_t s) {
   constexpr int G = kDecodeGroups, kRpc = kDecodeThreads / (D / (4 * G));
   const dim3 grid((a.B + kRpc - 1) / kRpc);
-  return launch_ex(c128_decode_kernel<D, InT, G, kDecodeMinBlocks>, grid, dim3(kDecodeThreads), 0, use_pdl, s,
+  if (a.cache)
+    return launch_ex(c128_decode_kernel<D, InT, G, kDecodeFp8MinBlocks, true>, grid, dim3(kDecodeThreads), 0,
+                     use_pdl, s, a);
+  return launch_ex(c128_decode_kernel<D, InT, G, kDecodeMinBlocks, false>, grid, dim3(kDecodeThreads), 0, use_pdl, s,
                    a);
 }
 
@@ -304,7 +357,10 @@ cudaError_t prefill_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
     }
     if (e == cudaErrorNotSupported) {
       const dim3 grid(static_cast<unsigned>(a.num_compress) * S);
-      e = launch_ex(c128_prefill_kernel<D, InT, false>, grid, dim3(kPrefillWarps * 32), 0, use_pdl, s, a);
+      e = a.cache ? launch_ex(c128_prefill_kernel<D, InT, false, true>, grid, dim3(kPrefillWarps * 32), 0, use_pdl, s,
+                              a)
+                  : launch_ex(c128_prefill_kernel<D, InT, false, false>, grid, dim3(kPrefillWarps * 32), 0, use_pdl,
+                              s, a);
     }
     if (e != cudaSuccess) return e;
   }
@@ -313,7 +369,7 @@ cudaError_t prefill_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
     C128PrefillArgs w = a;
     w.write_early = (use_pdl && a.num_compress) ? 1 : 0;
     cudaError_t e =
-        launch_ex(c128_prefill_kernel<D, InT, true>, grid, dim3(kPrefillWarps * 32), 0, use_pdl, s, w);
+        launch_ex(c128_prefill_kernel<D, InT, true, false>, grid, dim3(kPrefillWarps * 32), 0, use_pdl, s, w);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -205,14 +205,45 @@ ckv_status ckv_expand_pools_and_append_tail(const int32_t* pool_ids, int64_t poo
   return cuda_status(ckv::launch_expand_pools(a, use_pdl != 0, static_cast<cudaStream_t>(stream)));
 }
 
-ckv_status ckv_c128_online_decode(float* state, int64_t num_slots, const void* input,
-                                  ckv_dtype in_dtype, float* out, const float* ape,
-                                  const int32_t* indices, const int32_t* seq_lens, int32_t B,
-                                  int32_t D, int32_t use_pdl, int32_t* err_word, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The optional FP8 output stage of the c128 calls (kv_cache == nullptr: none).
+struct Fp8Out {
+  uint8_t* kv_cache;
+  int64_t num_pages;
+  int32_t page_size;
+  const int64_t* cache_loc;
+  int32_t round_scale;
+};
+
+ckv_status fp8_check(const Fp8Out* f) {
+  if (!f) return CKV_OK;
+  if (f->page_size <= 0 || f->num_pages < 0) return CKV_ERR_SHAPE;
+  if (!f->kv_cache || !f->cache_loc) return CKV_ERR_NULL;
+  if (!aligned(f->kv_cache, 16) || !aligned(f->cache_loc, 8)) return CKV_ERR_ALIGN;
+  return CKV_OK;
+}
+
+template <typename Args>
+void fp8_set(Args& a, const Fp8Out* f) {
+  if (!f) return;
+  a.cache = f->kv_cache;
+  a.cache_loc = f->cache_loc;
+  a.num_pages = f->num_pages;
+  a.page_size = f->page_size;
+  a.round_scale = f->round_scale;
+}
+
+ckv_status c128_decode_impl(float* state, int64_t num_slots, const void* input, ckv_dtype in_dtype, float* out,
+                            const float* ape, const int32_t* indices, const int32_t* seq_lens, int32_t B,
+                            int32_t D, const Fp8Out* fp8, int32_t use_pdl, int32_t* err_word, void* stream) {
   if (B < 0 || num_slots < 0 || !head_dim_ok(D)) return CKV_ERR_SHAPE;
   if (in_dtype != CKV_F32 && in_dtype != CKV_BF16) return CKV_ERR_DTYPE;
+  if (ckv_status c = fp8_check(fp8)) return c;
   if (B == 0) return CKV_OK;
-  if (!state || !input || !out || !ape || !indices || !seq_lens) return CKV_ERR_NULL;
+  if (!state || !input || !ape || !indices || !seq_lens || (!out && !fp8)) return CKV_ERR_NULL;
   if (!aligned(state, 16) || !aligned(input, 16) || !aligned(out, 16) || !aligned(ape, 16) ||
       !aligned(indices, 4) || !aligned(seq_lens, 4) || !aligned(err_word, 4))
     return CKV_ERR_ALIGN;
@@ -226,28 +257,28 @@ ckv_status ckv_c128_online_decode(float* state, int64_t num_slots, const void* i
   a.seq_lens = seq_lens;
   a.err = err_word;
   a.B = B;
+  fp8_set(a, fp8);
   return cuda_status(ckv::launch_c128_decode(a, D, in_dtype, use_pdl != 0,
                                              static_cast<cudaStream_t>(stream)));
 }
 
-ckv_status ckv_c128_online_prefill(float* state, int64_t num_slots, const void* input,
-                                   ckv_dtype in_dtype, int64_t num_tokens, float* out,
-                                   const float* ape, const int32_t* indices,
-                                   const int32_t* load_indices, int32_t B,
-                                   const ckv_plan_entry* compress_plan, uint32_t num_compress,
-                                   const ckv_plan_entry* write_plan, uint32_t num_write, int32_t D,
-                                   int32_t use_pdl, int32_t* err_word, void* stream) {
+ckv_status c128_prefill_impl(float* state, int64_t num_slots, const void* input, ckv_dtype in_dtype,
+                             int64_t num_tokens, float* out, const float* ape, const int32_t* indices,
+                             const int32_t* load_indices, int32_t B, const ckv_plan_entry* compress_plan,
+                             uint32_t num_compress, const ckv_plan_entry* write_plan, uint32_t num_write,
+                             int32_t D, const Fp8Out* fp8, int32_t use_pdl, int32_t* err_word, void* stream) {
   if (B < 0 || num_slots < 0 || num_tokens < 0 || num_tokens > static_cast<int64_t>(UINT32_MAX) ||
       !head_dim_ok(D))
     return CKV_ERR_SHAPE;
   if (in_dtype != CKV_F32 && in_dtype != CKV_BF16) return CKV_ERR_DTYPE;
+  if (ckv_status c = fp8_check(fp8)) return c;
   if (num_compress == 0 && num_write == 0) return CKV_OK;
   const uint64_t S = static_cast<uint64_t>(D / 128);
   if (static_cast<uint64_t>(num_compress) * S > static_cast<uint64_t>(INT32_MAX) ||
       static_cast<uint64_t>(num_write) * S > static_cast<uint64_t>(INT32_MAX))
     return CKV_ERR_SHAPE;
   if (!state || !input || !ape || !indices) return CKV_ERR_NULL;
-  if ((num_compress && (!compress_plan || !out)) || (num_write && !write_plan)) return CKV_ERR_NULL;
+  if ((num_compress && (!compress_plan || (!out && !fp8))) || (num_write && !write_plan)) return CKV_ERR_NULL;
   if (!aligned(state, 16) || !aligned(input, 16) || !aligned(out, 16) || !aligned(ape, 16) ||
       !aligned(compress_plan, 16) || !aligned(write_plan, 16) || !aligned(indices, 4) ||
       !aligned(load_indices, 4) || !aligned(err_word, 4))
@@ -267,8 +298,60 @@ ckv_status ckv_c128_online_prefill(float* state, int64_t num_slots, const void* 
   a.num_compress = num_compress;
   a.num_write = num_write;
   a.B = B;
+  fp8_set(a, fp8);
   return cuda_status(ckv::launch_c128_prefill(a, D, in_dtype, use_pdl != 0,
                                               static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+ckv_status ckv_c128_online_decode(float* state, int64_t num_slots, const void* input,
+                                  ckv_dtype in_dtype, float* out, const float* ape,
+                                  const int32_t* indices, const int32_t* seq_lens, int32_t B,
+                                  int32_t D, int32_t use_pdl, int32_t* err_word, void* stream) {
+  return c128_decode_impl(state, num_slots, input, in_dtype, out, ape, indices, seq_lens, B, D, nullptr, use_pdl,
+                          err_word, stream);
+}
+
+ckv_status ckv_c128_online_decode_fp8(float* state, int64_t num_slots, const void* input,
+                                      ckv_dtype in_dtype, float* out, const float* ape,
+                                      const int32_t* indices, const int32_t* seq_lens, int32_t B,
+                                      int32_t D, uint8_t* kv_cache, int64_t num_pages,
+                                      int32_t page_size, const int64_t* cache_loc,
+                                      int32_t round_scale, int32_t use_pdl, int32_t* err_word,
+                                      void* stream) {
+  const Fp8Out f{kv_cache, num_pages, page_size, cache_loc, round_scale};
+  return c128_decode_impl(state, num_slots, input, in_dtype, out, ape, indices, seq_lens, B, D, &f, use_pdl,
+                          err_word, stream);
+}
+
+ckv_status ckv_c128_online_prefill(float* state, int64_t num_slots, const void* input,
+                                   ckv_dtype in_dtype, int64_t num_tokens, float* out,
+                                   const float* ape, const int32_t* indices,
+                                   const int32_t* load_indices, int32_t B,
+                                   const ckv_plan_entry* compress_plan, uint32_t num_compress,
+                                   const ckv_plan_entry* write_plan, uint32_t num_write, int32_t D,
+                                   int32_t use_pdl, int32_t* err_word, void* stream) {
+  return c128_prefill_impl(state, num_slots, input, in_dtype, num_tokens, out, ape, indices, load_indices, B,
+                           compress_plan, num_compress, write_plan, num_write, D, nullptr, use_pdl, err_word,
+                           stream);
+}
+
+ckv_status ckv_c128_online_prefill_fp8(float* state, int64_t num_slots, const void* input,
+                                       ckv_dtype in_dtype, int64_t num_tokens, float* out,
+                                       const float* ape, const int32_t* indices,
+                                       const int32_t* load_indices, int32_t B,
+                                       const ckv_plan_entry* compress_plan, uint32_t num_compress,
+                                       const ckv_plan_entry* write_plan, uint32_t num_write,
+                                       int32_t D, uint8_t* kv_cache, int64_t num_pages,
+                                       int32_t page_size, const int64_t* cache_loc,
+                                       int32_t round_scale, int32_t use_pdl, int32_t* err_word,
+                                       void* stream) {
+  const Fp8Out f{kv_cache, num_pages, page_size, cache_loc, round_scale};
+  return c128_prefill_impl(state, num_slots, input, in_dtype, num_tokens, out, ape, indices, load_indices, B,
+                           compress_plan, num_compress, write_plan, num_write, D, &f, use_pdl, err_word, stream);
 }
 
 ckv_status ckv_c128_online_prefill_counted(float* state, int64_t num_slots, const void* input,

@@ -79,6 +79,15 @@ struct C128DecodeArgs {
   const int32_t* seq_lens;
   int32_t* err;
   int32_t B;
+  // optional FP8 output stage (cache == nullptr: none): every output row is
+  // also stored into a paged FP8 cache at location cache_loc[row], each
+  // 128-channel block bf16-rounded, Hadamard-rotated, bf16-rounded and
+  // absmax-quantised with its own fp32 scale
+  uint8_t* cache;
+  const int64_t* cache_loc;
+  int64_t num_pages;
+  int32_t page_size;
+  int32_t round_scale;
 };
 
 struct C128PrefillArgs {
@@ -99,6 +108,15 @@ struct C128PrefillArgs {
   uint32_t num_compress;
   uint32_t num_write;
   int32_t B;
+  // optional FP8 output stage (cache == nullptr: none): every output row is
+  // also stored into a paged FP8 cache at location cache_loc[row], each
+  // 128-channel block bf16-rounded, Hadamard-rotated, bf16-rounded and
+  // absmax-quantised with its own fp32 scale
+  uint8_t* cache;
+  const int64_t* cache_loc;
+  int64_t num_pages;
+  int32_t page_size;
+  int32_t round_scale;
   // write pass only, set by the launcher when the write launch is a
   // programmatic dependent of this call's own compress launch: everything
   // the write pass reads except the state was final before that launch began,

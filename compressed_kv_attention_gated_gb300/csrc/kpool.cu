@@ -23,6 +23,7 @@
 //
 // The pooled path is memory bound (no dense contraction); no tensor cores.
 #include "ckv_device.cuh"
+#include "ckv_fp8.cuh"
 #include "ckv_launch.h"
 #include "ckv_launch_util.cuh"
 #include "ckv_tma.cuh"
@@ -105,76 +106,6 @@ __device__ __forceinline__ void pool_softmax(const uint2 (&kr)[P], const uint2 (
     x[2 * h] = __fdividef(a0, d0);  // den in [1, P]
     x[2 * h + 1] = __fdividef(a1, d1);
   }
-}
-
-// x (fp32) -> bf16 -> Hadamard-128 (fp32) -> bf16 -> absmax FP8-e4m3 + scale.
-// The rotation is the orthonormal Sylvester Hadamard matrix: butterfly spans
-// 1, 2, 4, ..., 64 in ascending order, each (u + v, u - v) in fp32, then one
-// multiply by fp32(1/sqrt(128)).
-template <bool kRound>
-__device__ __forceinline__ void rotate_quantize(const float (&x)[4], int lane, uint32_t& codes,
-                                                float& scale, float (&xb)[4], float (&yb)[4]) {
-  float a[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    xb[i] = round_bf16(x[i]);
-    a[i] = xb[i];
-  }
-  {  // span 1: channel pairs (0,1), (2,3) of the lane
-    const float u0 = a[0], v0 = a[1], u1 = a[2], v1 = a[3];
-    a[0] = u0 + v0;
-    a[1] = u0 - v0;
-    a[2] = u1 + v1;
-    a[3] = u1 - v1;
-  }
-  {  // span 2: pairs (0,2), (1,3)
-    const float u0 = a[0], v0 = a[2], u1 = a[1], v1 = a[3];
-    a[0] = u0 + v0;
-    a[2] = u0 - v0;
-    a[1] = u1 + v1;
-    a[3] = u1 - v1;
-  }
-#pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {  // spans 4, 8, 16, 32, 64: partner lane l ^ m
-    // lower lane: a + o; upper lane: o - a.  fma(a, -1, o) rounds o - a once,
-    // exactly like a subtraction, so one FMA serves both halves.
-    const float sgn = (lane & m) ? -1.f : 1.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float o = __shfl_xor_sync(0xFFFFFFFFu, a[i], m);
-      a[i] = fmaf(a[i], sgn, o);
-    }
-  }
-  const float c = __uint_as_float(0x3DB504F3u);  // fp32(1/sqrt(128))
-  float am = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    yb[i] = round_bf16(a[i] * c);
-    am = fmaxf(am, fabsf(yb[i]));
-  }
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, m));
-  am = fmaxf(am, 1e-4f);
-  const float v = am * __uint_as_float(0x3B124925u);  // absmax * fp32(1/448)
-  float q[4];
-  if (kRound) {
-    // smallest power of two >= v (v is a positive normal number); dividing by a
-    // power of two is exact, so multiplying by its (exact) reciprocal is the same
-    // IEEE quotient
-    const uint32_t bits = __float_as_uint(v);
-    const uint32_t e = (bits & 0x007FFFFFu) ? (bits & 0x7F800000u) + 0x00800000u : (bits & 0x7F800000u);
-    scale = __uint_as_float(e);
-    const float inv = __uint_as_float((254u << 23) - e);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) q[i] = fminf(fmaxf(yb[i] * inv, -448.f), 448.f);
-  } else {
-    scale = v;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) q[i] = fminf(fmaxf(__fdiv_rn(yb[i], scale), -448.f), 448.f);
-  }
-  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(q[0], q[1]), __NV_SATFINITE, __NV_E4M3);
-  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(q[2], q[3]), __NV_SATFINITE, __NV_E4M3);
-  codes = (lo & 0xFFFFu) | (hi << 16);
 }
 
 __device__ __forceinline__ void write_taps(float* tx, uint16_t* txb, uint16_t* tyb, int64_t row,

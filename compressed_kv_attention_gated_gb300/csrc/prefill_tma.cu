@@ -32,6 +32,7 @@
 #include <mutex>
 
 #include "ckv_device.cuh"
+#include "ckv_fp8.cuh"
 #include "ckv_launch.h"
 #include "ckv_launch_util.cuh"
 #include "ckv_tma.cuh"
@@ -66,19 +67,20 @@ struct TmaCfg<__nv_bfloat16> {
 
 constexpr int kRowsPerWarp = 8;
 
-template <typename InT>
+template <typename InT, bool kFp8 = false>
 struct Layout {
   static constexpr int kCh = TmaCfg<InT>::kCh, kSt = TmaCfg<InT>::kStages;
   static constexpr int kCWarps = TmaCfg<InT>::kCWarps, kRows = TmaCfg<InT>::kRows;
   static constexpr int kRowBytes = kCh * static_cast<int>(sizeof(InT));
   static constexpr int kBoxBytes = kRows * kRowBytes;                 // one array, one stage
-  static constexpr int kThreads = (kCWarps + 1) * 32;                 // + the producer warp
+  static constexpr int kThreads = (kCWarps + 1 + (kFp8 ? 1 : 0)) * 32;  // + producer (+ FP8 warp)
   static constexpr int kKv = 0;
   static constexpr int kSc = kKv + kSt * kBoxBytes;
   static constexpr int kApe = kSc + kSt * kBoxBytes;                  // [128][kCh] fp32 * log2(e)
   static constexpr int kPart = kApe + 128 * kCh * 4;                  // [2][kCWarps][3][kCh] fp32
-  static constexpr int kBar = kPart + 2 * kCWarps * 3 * kCh * 4;     // full[kSt] empty[kSt] ready[2]
-  static constexpr int kBytes = kBar + (2 * kSt + 2) * 8;
+  static constexpr int kRow = kPart + 2 * kCWarps * 3 * kCh * 4;     // FP8 stage: [2][kCh] fp32
+  static constexpr int kBar = kRow + (kFp8 ? 2 * kCh * 4 : 0);       // full, empty, ready (, rowready, rowfree)
+  static constexpr int kBytes = kBar + (2 * kSt + 2 + (kFp8 ? 4 : 0)) * 8;
   static_assert(kRows == kCWarps * kRowsPerWarp, "each consumer warp owns 8 rows of a stage");
 };
 
@@ -143,11 +145,11 @@ __device__ __forceinline__ void load_ape(const float* ape_row, int lane, float (
   }
 }
 
-template <int D, typename InT>
-__global__ void __launch_bounds__(Layout<InT>::kThreads, 1)
+template <int D, typename InT, bool kFp8>
+__global__ void __launch_bounds__(Layout<InT, kFp8>::kThreads, 1)
     c128_prefill_tma_kernel(const __grid_constant__ CUtensorMap tmap,
                             const __grid_constant__ C128PrefillArgs a) {
-  using L = Layout<InT>;
+  using L = Layout<InT, kFp8>;
   constexpr int kCh = TmaCfg<InT>::kCh, kCpl = TmaCfg<InT>::kCpl, kSt = TmaCfg<InT>::kStages;
   constexpr int kCWarps = L::kCWarps, kRows = L::kRows, kBoxBytes = L::kBoxBytes;
   constexpr int kThreads = L::kThreads, kRowBytes = L::kRowBytes;
@@ -157,6 +159,8 @@ __global__ void __launch_bounds__(Layout<InT>::kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* empty = full + kSt;
   uint64_t* ready = empty + kSt;
+  uint64_t* rowready = ready + 2;  // FP8 stage only: a segment's row is staged
+  uint64_t* rowfree = ready + 4;   // FP8 stage only: the FP8 warp has read it
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slice = blockIdx.x % S;
@@ -169,6 +173,12 @@ __global__ void __launch_bounds__(Layout<InT>::kThreads, 1)
     }
     mbar_init(&ready[0], kCWarps);
     mbar_init(&ready[1], kCWarps);
+    if constexpr (kFp8) {
+      mbar_init(&rowready[0], kCh / 32);
+      mbar_init(&rowready[1], kCh / 32);
+      mbar_init(&rowfree[0], 1);
+      mbar_init(&rowfree[1], 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();  // barriers initialised before anyone waits on them
@@ -213,10 +223,55 @@ __global__ void __launch_bounds__(Layout<InT>::kThreads, 1)
     return;
   }
 
+  if constexpr (kFp8) {
+    if (warp == kCWarps + 1) {
+      // ---------------------------------------------------------- FP8 warp
+      // takes each segment's staged row (block `slice` of the output row) and
+      // stores it through the pooled output stage, while the consumers go on
+      pdl_trigger();
+      uint32_t it = 0;
+      uint4 next = load_plan(a.compress_plan, group, n);
+      for (uint32_t p = group; p < n; p += ngroups) {
+        const uint4 cur = next;
+        next = load_plan(a.compress_plan, p + ngroups, n);
+        const Seg s = decode_plan(cur, a);
+        if (!s.ok) continue;  // the consumers skip it too
+        const int buf = static_cast<int>(it & 1);
+        const uint32_t par = (it >> 1) & 1;
+        ++it;
+        bool slot_ok = true;
+        if (s.pic + 1 != s.window) {
+          const int32_t li = a.load_indices[s.batch];
+          slot_ok = li >= 0 && li < a.num_slots;
+        }
+        const int64_t loc = a.cache_loc[s.ragged];
+        if (!mbar_wait(&rowready[buf], par)) {
+          if (lane == 0) flag_error(a.err, CKV_DEVERR_TIMEOUT);
+          return;
+        }
+        const float4 v = reinterpret_cast<const float4*>(smem + L::kRow + buf * kCh * 4)[lane];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rowfree[buf]);
+        if (!slot_ok) continue;
+        if (loc < 0 || loc >= a.num_pages * a.page_size) {
+          if (lane == 0 && slice == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
+          continue;
+        }
+        const float x[4] = {v.x, v.y, v.z, v.w};
+        float xb[4], yb[4], scale;
+        uint32_t codes;
+        if (a.round_scale) rotate_quantize<true>(x, lane, codes, scale, xb, yb);
+        else rotate_quantize<false>(x, lane, codes, scale, xb, yb);
+        cache_write_block(a.cache, a.page_size, loc, S, slice, lane, codes, scale);
+      }
+      return;
+    }
+  }
+
   // -------------------------------------------------------------- consumers
   // bias slice, pre-scaled to the log2 domain, staged by the consumer warps
   // (named barrier 1) while the producer's first loads are in flight
-  for (int i = threadIdx.x - 32; i < 128 * kCh / 4; i += kThreads - 32) {
+  for (int i = threadIdx.x - 32; i < 128 * kCh / 4; i += kCWarps * 32) {
     const int j = i / (kCh / 4), c4 = i % (kCh / 4);
     float4 v = ld_shared_ro_f4(a.ape + j * D + slice * kCh + 4 * c4);
     v.x *= kLog2e;
@@ -348,11 +403,21 @@ __global__ void __launch_bounds__(Layout<InT>::kThreads, 1)
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&ready[buf]);
-    if (!mbar_wait(&ready[buf], (it >> 1) & 1)) {
+    const uint32_t seg_parity = (it >> 1) & 1;
+    if (!mbar_wait(&ready[buf], seg_parity)) {
       if (lane == 0) flag_error(a.err, CKV_DEVERR_TIMEOUT);
       return;
     }
     ++it;
+    if constexpr (kFp8) {
+      // the row buffer of this parity was last used two segments ago: wait
+      // until the FP8 warp has read it
+      const uint32_t use = (it - 1) >> 1;  // this segment's use of buffer `buf`
+      if (cw < kCh / 32 && use > 0 && !mbar_wait(&rowfree[buf], (use - 1) & 1)) {
+        if (lane == 0) flag_error(a.err, CKV_DEVERR_TIMEOUT);
+        return;
+      }
+    }
     if (t < kCh && slot_ok) {
       float m = kNegBig;
 #pragma unroll
@@ -371,7 +436,15 @@ __global__ void __launch_bounds__(Layout<InT>::kThreads, 1)
         const float w1 = s1 * fast_exp2(m1l - nm), w2 = ssum * fast_exp2(m - nm);
         kvout = (k1 * w1 + kvout * w2) / (w1 + w2);
       }
-      a.out[static_cast<int64_t>(s.ragged) * D + slice * kCh + t] = kvout;
+      if (a.out) a.out[static_cast<int64_t>(s.ragged) * D + slice * kCh + t] = kvout;
+      if constexpr (kFp8) reinterpret_cast<float*>(smem + L::kRow)[buf * kCh + t] = kvout;
+    }
+    if constexpr (kFp8) {
+      // the epilogue warps hand the row slice to the FP8 warp
+      if (cw < kCh / 32) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rowready[buf]);
+      }
     }
   }
 }
@@ -401,10 +474,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+template <int D, typename InT, bool kFp8>
+cudaError_t launch_grid(const CUtensorMap& map, const C128PrefillArgs& a, int sms, bool use_pdl, cudaStream_t s);
+
 template <int D, typename InT>
 cudaError_t launch_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
   using Cfg = TmaCfg<InT>;
-  constexpr int S = D / Cfg::kCh;
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   CUtensorMap map;
@@ -421,14 +496,22 @@ cudaError_t launch_d(const C128PrefillArgs& a, bool use_pdl, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  auto kern = c128_prefill_tma_kernel<D, InT>;
-  e = set_max_smem_once<c128_prefill_tma_kernel<D, InT>>(Layout<InT>::kBytes);
+  if (a.cache) return launch_grid<D, InT, true>(map, a, sms, use_pdl, s);
+  return launch_grid<D, InT, false>(map, a, sms, use_pdl, s);
+}
+
+template <int D, typename InT, bool kFp8>
+cudaError_t launch_grid(const CUtensorMap& map, const C128PrefillArgs& a, int sms, bool use_pdl, cudaStream_t s) {
+  using L = Layout<InT, kFp8>;
+  constexpr int S = D / TmaCfg<InT>::kCh;
+  auto kern = c128_prefill_tma_kernel<D, InT, kFp8>;
+  cudaError_t e = set_max_smem_once<c128_prefill_tma_kernel<D, InT, kFp8>>(L::kBytes);
   if (e != cudaSuccess) return e;
   const int grid = sms >= S ? (sms / S) * S : S;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(Layout<InT>::kThreads);
-  cfg.dynamicSmemBytes = Layout<InT>::kBytes;
+  cfg.blockDim = dim3(L::kThreads);
+  cfg.dynamicSmemBytes = L::kBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -305,6 +305,48 @@ ckv_status ckv_plan_online_prefill(const int64_t* seq_lens, const int64_t* exten
                                    uint32_t* num_compress, uint32_t* num_write);
 
 /*
+ * The c128 calls with an FP8 output stage: every compressed row the call
+ * emits (decode: the rows of chunk-closing requests; prefill: the compress
+ * rows) is also stored into a paged FP8 cache, the way the pooled path stores
+ * its rows -- the combination of the sglang c128_online.cuh page's
+ * compressed rows with the quantisation stage of the vLLM kpool_compress
+ * page (_kpool_softmax_rotate_write_cache_kernel).  Neither page shows this
+ * combination; the readings taken:
+ *   - the row's D channels are D/128 blocks of 128, and each block is treated
+ *     exactly like one pooled vector: fp32 -> bf16 (round to nearest even) ->
+ *     Hadamard-128 (the pooled path's rotation) -> bf16 -> absmax FP8-e4m3 with
+ *     its own fp32 scale (round_scale as for the pooled calls);
+ *   - kv_cache  device uint8 [num_pages][page_size][D + 4*(D/128)]: per page,
+ *     page_size rows of D FP8 bytes (block j at bytes 128j..128j+127), then
+ *     page_size*(D/128) fp32 scales (row r, block j at r*(D/128) + j); with
+ *     D = 128 this is the pooled cache layout.
+ * cache_loc   device int64: decode [B], the cache row of request b when its
+ *             chunk closes; prefill [num_tokens], read at the ragged row of
+ *             each compress segment.  A location outside
+ *             [0, num_pages*page_size) sets CKV_DEVERR_CACHE_LOC and is skipped.
+ * out         may be NULL here (only the FP8 rows are produced); otherwise as
+ *             for ckv_c128_online_decode / ckv_c128_online_prefill.
+ * All other arguments and the state update are those of the plain calls.
+ */
+ckv_status ckv_c128_online_decode_fp8(float* state, int64_t num_slots, const void* input,
+                                      ckv_dtype in_dtype, float* out, const float* ape,
+                                      const int32_t* indices, const int32_t* seq_lens, int32_t B,
+                                      int32_t D, uint8_t* kv_cache, int64_t num_pages,
+                                      int32_t page_size, const int64_t* cache_loc,
+                                      int32_t round_scale, int32_t use_pdl, int32_t* err_word,
+                                      void* stream);
+ckv_status ckv_c128_online_prefill_fp8(float* state, int64_t num_slots, const void* input,
+                                       ckv_dtype in_dtype, int64_t num_tokens, float* out,
+                                       const float* ape, const int32_t* indices,
+                                       const int32_t* load_indices, int32_t B,
+                                       const ckv_plan_entry* compress_plan, uint32_t num_compress,
+                                       const ckv_plan_entry* write_plan, uint32_t num_write,
+                                       int32_t D, uint8_t* kv_cache, int64_t num_pages,
+                                       int32_t page_size, const int64_t* cache_loc,
+                                       int32_t round_scale, int32_t use_pdl, int32_t* err_word,
+                                       void* stream);
+
+/*
  * Device-side planner: the same plans as ckv_plan_online_prefill (sglang
  * c128_online.cuh page, plan_online_prefill_host), computed by a CUDA kernel
  * on `stream`, so that planning and the prefill can be enqueued -- or

@@ -1,0 +1,182 @@
+"""c128 rows with the FP8 output stage (ckv_c128_online_decode_fp8,
+ckv_c128_online_prefill_fp8): the sglang c128_online.cuh page's compressed
+rows taken, 128-channel block by block, through the vLLM kpool_compress
+page's output stage into a paged FP8 cache.
+
+For every call: the state and fp32 rows equal the plain call's bit for bit;
+every byte of the cache equals the oracle's store of the GPU's own fp32 rows
+(bf16, Hadamard-128, bf16 and absmax FP8 are deterministic given the fp32
+row, so this is exact), bytes of other rows keep their canary; leaving out
+the fp32 rows gives the same cache; a bad location is flagged and skipped."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import assert_close_rel, bf16_bits, f32, u8
+
+pytestmark = pytest.mark.gpu
+CANARY = 0x5A
+
+
+@pytest.fixture(scope="module")
+def ck():
+    import compressed_kv_attention_gated_gb300 as ck
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ck.load()
+    return ck
+
+
+@pytest.fixture(params=[1, 2], ids=["cta_per_segment", "tma_pipeline"])
+def variant(request, ck):
+    prev = ck.ckv_c128_prefill_set_variant(request.param)
+    yield request.param
+    ck.ckv_c128_prefill_set_variant(prev)
+
+
+def _cache(rows, D, ps=16):
+    pages = (rows + ps - 1) // ps + 1
+    return torch.full((pages, ps, D + 4 * (D // 128)), CANARY, dtype=torch.uint8), ps
+
+
+def _expect(ora, cache0, ps, rows, locs, round_scale):
+    ref = u8(cache0).copy()
+    ora.c128_rows_to_cache(ref, ps, rows, locs, round_scale=round_scale)
+    return ref
+
+
+def _input_np(t):
+    return bf16_bits(t) if t.dtype == torch.bfloat16 else f32(t)
+
+
+@pytest.mark.parametrize("round_scale", [True, False])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("D", [128, 256, 512])
+def test_decode_fp8(ck, ora, D, dtype, round_scale):
+    from compressed_kv_attention_gated_gb300 import synth
+
+    B = 301
+    d = synth.c128_decode("cpu", seed=D + 2 * (dtype == torch.bfloat16), B=B, D=D, num_slots=700, dtype=dtype)
+    seq = d["seq_lens"].clone()
+    seq[::3] = (seq[::3] // 128 + 1) * 128  # a third of the requests close their chunk
+    d["seq_lens"] = seq
+    closed = ((seq.numpy().astype(np.int64) - 1) % 128) == 127
+    g = torch.Generator().manual_seed(D)
+    cache0, ps = _cache(2 * B, D)
+    cache_loc = torch.randperm(cache0.shape[0] * ps, generator=g)[:B].to(torch.int64)
+    dev = "cuda"
+    args = [d["input"].to(dev), None, d["ape"].to(dev), d["indices"].to(dev), d["seq_lens"].to(dev)]
+    # plain call
+    st_p = d["state"].to(dev).clone()
+    out_p = torch.zeros((B, D), device=dev)
+    ck.ckv_c128_online_decode(st_p, args[0], out_p, *args[2:])
+    # FP8 stage with and without the fp32 rows
+    err = torch.zeros((1,), dtype=torch.int32, device=dev)
+    st_f, out_f, cache = d["state"].to(dev).clone(), torch.zeros((B, D), device=dev), cache0.to(dev)
+    ck.ckv_c128_online_decode_fp8(st_f, args[0], out_f, *args[2:], cache, cache_loc.to(dev),
+                                  round_scale=round_scale, use_pdl=True, err_word=err)
+    st_n, cache_n = d["state"].to(dev).clone(), cache0.to(dev)
+    ck.ckv_c128_online_decode_fp8(st_n, args[0], None, *args[2:], cache_n, cache_loc.to(dev),
+                                  round_scale=round_scale, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(f32(st_f).view(np.uint32), f32(st_p).view(np.uint32))
+    assert np.array_equal(f32(st_n).view(np.uint32), f32(st_p).view(np.uint32))
+    assert np.array_equal(f32(out_f)[closed].view(np.uint32), f32(out_p)[closed].view(np.uint32))
+    out_ref, _, cl = ora.c128_decode(f32(d["state"]), _input_np(d["input"]), f32(d["ape"]), d["indices"].numpy(),
+                                     d["seq_lens"].numpy())
+    assert np.array_equal(cl, closed) and closed.sum() > 50
+    assert_close_rel(f32(out_f)[closed], out_ref[closed], "closing rows")
+    ref = _expect(ora, cache0, ps, f32(out_f)[closed], cache_loc.numpy()[closed], round_scale)
+    np.testing.assert_array_equal(u8(cache), ref)
+    np.testing.assert_array_equal(u8(cache_n), ref)
+
+
+def _prefill(ck, d, cp, wp, nc, nw, out, cache, cache_loc, round_scale, use_pdl, err, fp8=True):
+    dev = "cuda"
+    state = d["state"].to(dev).clone()
+    common = (state, d["input"].to(dev), out, d["ape"].to(dev), d["indices"].to(dev), cp.to(dev), nc,
+              wp.to(dev), nw)
+    if fp8:
+        ck.ckv_c128_online_prefill_fp8(*common, cache, cache_loc.to(dev), round_scale=round_scale, use_pdl=use_pdl,
+                                       err_word=err)
+    else:
+        ck.ckv_c128_online_prefill(*common, use_pdl=use_pdl, err_word=err)
+    return state
+
+
+@pytest.mark.parametrize("use_pdl", [False, True])
+@pytest.mark.parametrize("round_scale", [True, False])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("D", [128, 512])
+def test_prefill_fp8(variant, ck, ora, D, dtype, round_scale, use_pdl):
+    from compressed_kv_attention_gated_gb300 import synth
+
+    d = synth.c128_prefill("cpu", seed=7 + D, B=11, D=D, max_prefix=700, max_extend=900, dtype=dtype)
+    T = d["num_tokens"]
+    cp, wp, nc, nw = ck.ckv_plan_online_prefill(d["seq_lens"], d["extend_lens"])
+    rows = cp[:nc].view(torch.int32).view(-1, 4)[:, 0].numpy().astype(np.int64)
+    cache0, ps = _cache(T, D)
+    cache_loc = torch.randperm(cache0.shape[0] * ps, generator=torch.Generator().manual_seed(D))[:T].to(torch.int64)
+    dev = "cuda"
+    err = torch.zeros((1,), dtype=torch.int32, device=dev)
+    out_p = torch.zeros((T, D), device=dev)
+    st_p = _prefill(ck, d, cp, wp, nc, nw, out_p, None, None, round_scale, use_pdl, err, fp8=False)
+    out_f, cache = torch.zeros((T, D), device=dev), cache0.to(dev)
+    st_f = _prefill(ck, d, cp, wp, nc, nw, out_f, cache, cache_loc, round_scale, use_pdl, err)
+    cache_n = cache0.to(dev)
+    st_n = _prefill(ck, d, cp, wp, nc, nw, None, cache_n, cache_loc, round_scale, use_pdl, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and nc > 10
+    for st in (st_f, st_n):
+        assert np.array_equal(f32(st).view(np.uint32), f32(st_p).view(np.uint32))
+    assert np.array_equal(f32(out_f)[rows].view(np.uint32), f32(out_p)[rows].view(np.uint32))
+    ref = _expect(ora, cache0, ps, f32(out_f)[rows], cache_loc.numpy()[rows], round_scale)
+    np.testing.assert_array_equal(u8(cache), ref)
+    np.testing.assert_array_equal(u8(cache_n), ref)
+
+
+def test_prefill_fp8_long_context_full(ck, ora):
+    """8 x 131,072 bf16 tokens (8192 compress rows, TMA pipeline by default)."""
+    from compressed_kv_attention_gated_gb300 import synth
+
+    d = synth.long_context("cuda", seed=3)
+    T = d["num_tokens"]
+    cp, wp, nc, nw = ck.ckv_plan_online_prefill(d["seq_lens"], d["extend_lens"])
+    rows = np.arange(127, T, 128)
+    cache0, ps = _cache(nc, 512, ps=64)
+    cache_loc = torch.full((T,), -1, dtype=torch.int64)
+    cache_loc[torch.from_numpy(rows)] = torch.randperm(nc, generator=torch.Generator().manual_seed(1))
+    err = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    out = torch.zeros((T, 512), device="cuda")
+    cache = cache0.cuda()
+    ck.ckv_c128_online_prefill_fp8(d["state"], d["input"], out, d["ape"], d["indices"], cp.cuda(), nc, wp.cuda(), nw,
+                                   cache, cache_loc.cuda(), use_pdl=True, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    g = f32(out.index_select(0, torch.from_numpy(rows).cuda()))
+    ref = _expect(ora, cache0, ps, g, cache_loc.numpy()[rows], True)
+    np.testing.assert_array_equal(u8(cache), ref)
+
+
+def test_fp8_bad_location_flagged_and_skipped(ck, ora):
+    from compressed_kv_attention_gated_gb300 import synth
+
+    B, D = 64, 256
+    d = synth.c128_decode("cpu", seed=5, B=B, D=D, num_slots=128)
+    d["seq_lens"] = torch.full((B,), 128, dtype=torch.int32)  # every request closes
+    cache0, ps = _cache(B, D)
+    cache_loc = torch.arange(B, dtype=torch.int64)
+    cache_loc[3] = -2
+    cache_loc[7] = cache0.shape[0] * ps  # one past the end
+    err = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    out, cache = torch.zeros((B, D), device="cuda"), cache0.cuda()
+    ck.ckv_c128_online_decode_fp8(d["state"].cuda().clone(), d["input"].cuda(), out, d["ape"].cuda(),
+                                  d["indices"].cuda(), d["seq_lens"].cuda(), cache, cache_loc.cuda(), err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0x4  # CKV_DEVERR_CACHE_LOC
+    good = np.ones(B, bool)
+    good[[3, 7]] = False
+    ref = _expect(ora, cache0, ps, f32(out)[good], cache_loc.numpy()[good], True)
+    np.testing.assert_array_equal(u8(cache), ref)
