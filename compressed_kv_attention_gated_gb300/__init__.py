@@ -11,6 +11,7 @@ from .ckv import (  # noqa: F401
     ckv_c128_online_prefill,
     ckv_c128_online_prefill_fp8,
     ckv_c128_online_prefill_counted,
+    ckv_c128_online_prefill_counted_fp8,
     ckv_c128_prefill_set_variant,
     ckv_check_distinct,
     ckv_check_distinct_noalloc,

@@ -35,6 +35,7 @@ _STATUS_FUNCS = {
     "ckv_plan_online_prefill": 9,
     "ckv_plan_online_prefill_device": 11,
     "ckv_c128_online_prefill_counted": 17,
+    "ckv_c128_online_prefill_counted_fp8": 22,
     "ckv_expand_pools_and_append_tail": 9,
     "ckv_wait_timeout_selftest": 3,
     "ckv_check_distinct": 8,
@@ -118,6 +119,12 @@ def load():
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                ctypes.c_void_p, ctypes.c_void_p]
+            L.ckv_c128_online_prefill_counted_fp8.argtypes = [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                 ctypes.c_void_p, ctypes.c_void_p]
             L.ckv_expand_pools_and_append_tail.argtypes = [
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
@@ -490,6 +497,35 @@ def ckv_c128_online_prefill_counted(state, input, out, ape, indices, compress_pl
         _ptr(state), state.numel() // (3 * D), _ptr(input), _dtype(input), T, _ptr(out), _ptr(ape), _ptr(indices),
         _ptr(load_indices), B, _ptr(compress_plan), _ptr(write_plan), _ptr(counts), D, int(bool(use_pdl)),
         _ptr(err_word), _stream(stream, input)))
+
+
+def ckv_c128_online_prefill_counted_fp8(state, input, out, ape, indices, compress_plan, write_plan, counts,
+                                        kv_cache, cache_loc, round_scale=True, load_indices=None, use_pdl=False,
+                                        err_word=None, stream=None):
+    """The device-counted prefill with the FP8 output stage; see include/ckv.h.
+    kv_cache uint8 [pages, page_size, D + 4*D/128]; cache_loc int64 [T]; out
+    float32 [T, D] or None."""
+    L = load()
+    _cuda("ckv_c128_online_prefill_counted_fp8", state, input, out, ape, indices, load_indices, compress_plan,
+          write_plan, counts, kv_cache, cache_loc, err_word)
+    T = input.shape[0]
+    D = input.shape[1] // 2
+    B = indices.numel()
+    _need(state.dtype == torch.float32 and state.is_contiguous() and state.numel() % (3 * D) == 0,
+          "state must be contiguous float32 [slots, 3, D]")
+    _need(input.is_contiguous() and input.dim() == 2, "input must be contiguous [T, 2D]")
+    _need(out is None or (out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (T, D)),
+          "out must be float32 [T, D] or None")
+    _need(ape.dtype == torch.float32 and ape.is_contiguous() and tuple(ape.shape) == (128, D), "ape must be float32 [128, D]")
+    _need(indices.dtype == torch.int32 and indices.is_contiguous(), "indices must be int32 [B]")
+    for pl in (compress_plan, write_plan):
+        _need(pl.is_contiguous() and pl.numel() * pl.element_size() >= min(T, T // 128 + B) * PLAN_ENTRY_BYTES,
+              "plan tensors too small")
+    pages, ps = _fp8_cache(kv_cache, cache_loc, D, T)
+    _check("ckv_c128_online_prefill_counted_fp8", L.ckv_c128_online_prefill_counted_fp8(
+        _ptr(state), state.numel() // (3 * D), _ptr(input), _dtype(input), T, _ptr(out), _ptr(ape), _ptr(indices),
+        _ptr(load_indices), B, _ptr(compress_plan), _ptr(write_plan), _ptr(counts), D, _ptr(kv_cache), pages, ps,
+        _ptr(cache_loc), int(bool(round_scale)), int(bool(use_pdl)), _ptr(err_word), _stream(stream, input)))
 
 
 def ckv_plan_online_prefill(seq_lens, extend_lens, num_tokens=None, pad_for_graph=False,

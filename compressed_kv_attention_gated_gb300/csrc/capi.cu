@@ -303,6 +303,51 @@ ckv_status c128_prefill_impl(float* state, int64_t num_slots, const void* input,
                                               static_cast<cudaStream_t>(stream)));
 }
 
+ckv_status c128_prefill_counted_impl(float* state, int64_t num_slots, const void* input, ckv_dtype in_dtype,
+                                     int64_t num_tokens, float* out, const float* ape, const int32_t* indices,
+                                     const int32_t* load_indices, int32_t B, const ckv_plan_entry* compress_plan,
+                                     const ckv_plan_entry* write_plan, const uint32_t* counts, int32_t D,
+                                     const Fp8Out* fp8, int32_t use_pdl, int32_t* err_word, void* stream) {
+  if (B < 0 || num_slots < 0 || num_tokens < 0 || num_tokens > static_cast<int64_t>(UINT32_MAX) ||
+      !head_dim_ok(D))
+    return CKV_ERR_SHAPE;
+  if (in_dtype != CKV_F32 && in_dtype != CKV_BF16) return CKV_ERR_DTYPE;
+  if (ckv_status c = fp8_check(fp8)) return c;
+  if (num_tokens == 0 || B == 0) return CKV_OK;
+  // every compress segment closes a chunk: per request at most extend/128 + 1 of
+  // them, so at most num_tokens/128 + B in total; at most one write segment each
+  const uint64_t max_c = std::min<uint64_t>(static_cast<uint64_t>(num_tokens) / 128 + B,
+                                            static_cast<uint64_t>(num_tokens));
+  const uint64_t max_w = std::min<uint64_t>(B, static_cast<uint64_t>(num_tokens));
+  const uint64_t S = static_cast<uint64_t>(D / 128);
+  if (max_c * S > static_cast<uint64_t>(INT32_MAX)) return CKV_ERR_SHAPE;
+  if (!state || !input || !ape || !indices || (!out && !fp8) || !compress_plan || !write_plan || !counts)
+    return CKV_ERR_NULL;
+  if (!aligned(state, 16) || !aligned(input, 16) || !aligned(out, 16) || !aligned(ape, 16) ||
+      !aligned(compress_plan, 16) || !aligned(write_plan, 16) || !aligned(counts, 4) ||
+      !aligned(indices, 4) || !aligned(load_indices, 4) || !aligned(err_word, 4))
+    return CKV_ERR_ALIGN;
+  ckv::C128PrefillArgs a{};
+  a.state = state;
+  a.num_slots = num_slots;
+  a.input = input;
+  a.num_tokens = num_tokens;
+  a.out = out;
+  a.ape = ape;
+  a.indices = indices;
+  a.load_indices = load_indices ? load_indices : indices;
+  a.compress_plan = compress_plan;
+  a.write_plan = write_plan;
+  a.counts = counts;
+  a.err = err_word;
+  a.num_compress = static_cast<uint32_t>(max_c);
+  a.num_write = static_cast<uint32_t>(max_w);
+  a.B = B;
+  fp8_set(a, fp8);
+  return cuda_status(ckv::launch_c128_prefill(a, D, in_dtype, use_pdl != 0,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -362,42 +407,23 @@ ckv_status ckv_c128_online_prefill_counted(float* state, int64_t num_slots, cons
                                            const ckv_plan_entry* write_plan, const uint32_t* counts,
                                            int32_t D, int32_t use_pdl, int32_t* err_word,
                                            void* stream) {
-  if (B < 0 || num_slots < 0 || num_tokens < 0 || num_tokens > static_cast<int64_t>(UINT32_MAX) ||
-      !head_dim_ok(D))
-    return CKV_ERR_SHAPE;
-  if (in_dtype != CKV_F32 && in_dtype != CKV_BF16) return CKV_ERR_DTYPE;
-  if (num_tokens == 0 || B == 0) return CKV_OK;
-  // every compress segment closes a chunk: per request at most extend/128 + 1 of
-  // them, so at most num_tokens/128 + B in total; at most one write segment each
-  const uint64_t max_c = std::min<uint64_t>(static_cast<uint64_t>(num_tokens) / 128 + B,
-                                            static_cast<uint64_t>(num_tokens));
-  const uint64_t max_w = std::min<uint64_t>(B, static_cast<uint64_t>(num_tokens));
-  const uint64_t S = static_cast<uint64_t>(D / 128);
-  if (max_c * S > static_cast<uint64_t>(INT32_MAX)) return CKV_ERR_SHAPE;
-  if (!state || !input || !ape || !indices || !out || !compress_plan || !write_plan || !counts)
-    return CKV_ERR_NULL;
-  if (!aligned(state, 16) || !aligned(input, 16) || !aligned(out, 16) || !aligned(ape, 16) ||
-      !aligned(compress_plan, 16) || !aligned(write_plan, 16) || !aligned(counts, 4) ||
-      !aligned(indices, 4) || !aligned(load_indices, 4) || !aligned(err_word, 4))
-    return CKV_ERR_ALIGN;
-  ckv::C128PrefillArgs a{};
-  a.state = state;
-  a.num_slots = num_slots;
-  a.input = input;
-  a.num_tokens = num_tokens;
-  a.out = out;
-  a.ape = ape;
-  a.indices = indices;
-  a.load_indices = load_indices ? load_indices : indices;
-  a.compress_plan = compress_plan;
-  a.write_plan = write_plan;
-  a.counts = counts;
-  a.err = err_word;
-  a.num_compress = static_cast<uint32_t>(max_c);
-  a.num_write = static_cast<uint32_t>(max_w);
-  a.B = B;
-  return cuda_status(ckv::launch_c128_prefill(a, D, in_dtype, use_pdl != 0,
-                                              static_cast<cudaStream_t>(stream)));
+  return c128_prefill_counted_impl(state, num_slots, input, in_dtype, num_tokens, out, ape, indices, load_indices,
+                                   B, compress_plan, write_plan, counts, D, nullptr, use_pdl, err_word, stream);
+}
+
+ckv_status ckv_c128_online_prefill_counted_fp8(float* state, int64_t num_slots, const void* input,
+                                               ckv_dtype in_dtype, int64_t num_tokens, float* out,
+                                               const float* ape, const int32_t* indices,
+                                               const int32_t* load_indices, int32_t B,
+                                               const ckv_plan_entry* compress_plan,
+                                               const ckv_plan_entry* write_plan,
+                                               const uint32_t* counts, int32_t D, uint8_t* kv_cache,
+                                               int64_t num_pages, int32_t page_size,
+                                               const int64_t* cache_loc, int32_t round_scale,
+                                               int32_t use_pdl, int32_t* err_word, void* stream) {
+  const Fp8Out f{kv_cache, num_pages, page_size, cache_loc, round_scale};
+  return c128_prefill_counted_impl(state, num_slots, input, in_dtype, num_tokens, out, ape, indices, load_indices,
+                                   B, compress_plan, write_plan, counts, D, &f, use_pdl, err_word, stream);
 }
 
 ckv_status ckv_plan_online_prefill_device(const int64_t* seq_lens, const int64_t* extend_lens,

@@ -424,6 +424,22 @@ ckv_status ckv_check_distinct(const void* ids, int32_t id_bytes, int64_t n, int6
 ckv_status ckv_check_distinct_noalloc(const void* ids, int32_t id_bytes, int64_t n, int64_t range,
                                       int32_t* err_word, void* stream);
 
+/*
+ * ckv_c128_online_prefill_counted with the FP8 output stage of
+ * ckv_c128_online_prefill_fp8 (same readings, cache layout and cache_loc,
+ * read at the ragged row of each compress segment; out may be NULL).
+ */
+ckv_status ckv_c128_online_prefill_counted_fp8(float* state, int64_t num_slots, const void* input,
+                                               ckv_dtype in_dtype, int64_t num_tokens, float* out,
+                                               const float* ape, const int32_t* indices,
+                                               const int32_t* load_indices, int32_t B,
+                                               const ckv_plan_entry* compress_plan,
+                                               const ckv_plan_entry* write_plan,
+                                               const uint32_t* counts, int32_t D, uint8_t* kv_cache,
+                                               int64_t num_pages, int32_t page_size,
+                                               const int64_t* cache_loc, int32_t round_scale,
+                                               int32_t use_pdl, int32_t* err_word, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -180,3 +180,57 @@ def test_fp8_bad_location_flagged_and_skipped(ck, ora):
     good[[3, 7]] = False
     ref = _expect(ora, cache0, ps, f32(out)[good], cache_loc.numpy()[good], True)
     np.testing.assert_array_equal(u8(cache), ref)
+
+
+def test_counted_fp8_captured_with_device_planner(variant, ck, ora):
+    """Device planner + counted FP8 prefill captured in one CUDA graph and
+    replayed: identical to the host-planned FP8 call, cache equal to the oracle's."""
+    from compressed_kv_attention_gated_gb300 import synth
+
+    D = 256
+    d = synth.c128_prefill("cpu", seed=43, B=23, D=D, max_prefix=900, max_extend=1500)
+    T = d["num_tokens"]
+    dev = "cuda"
+    seq, ext = d["seq_lens"].to(dev), d["extend_lens"].to(dev)
+    cp = torch.empty((T, 16), dtype=torch.uint8, device=dev)
+    wp = torch.empty((T, 16), dtype=torch.uint8, device=dev)
+    cnt = torch.zeros((2,), dtype=torch.int32, device=dev)
+    cache0, ps = _cache(T, D)
+    cache_loc = torch.randperm(cache0.shape[0] * ps, generator=torch.Generator().manual_seed(3))[:T].to(torch.int64)
+    inp, ape, idx, loc = d["input"].to(dev), d["ape"].to(dev), d["indices"].to(dev), cache_loc.to(dev)
+    state0 = d["state"].to(dev)
+    state, out, cache = state0.clone(), torch.zeros((T, D), device=dev), cache0.to(dev)
+    err = torch.zeros((1,), dtype=torch.int32, device=dev)
+
+    def body():
+        ck.ckv_plan_online_prefill_device(seq, ext, T, compress_plan=cp, write_plan=wp, counts=cnt, err_word=err)
+        ck.ckv_c128_online_prefill_counted_fp8(state, inp, out, ape, idx, cp, wp, cnt, cache, loc, use_pdl=True,
+                                               err_word=err)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        body()  # set-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    state.copy_(state0)
+    out.zero_()
+    cache.copy_(cache0.to(dev))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        body()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    # host-planned FP8 call on fresh buffers
+    hcp, hwp, nc, nw = ck.ckv_plan_online_prefill(d["seq_lens"], d["extend_lens"])
+    out_h, cache_h = torch.zeros((T, D), device=dev), cache0.to(dev)
+    st_h = _prefill(ck, d, hcp, hwp, nc, nw, out_h, cache_h, cache_loc, True, True, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rows = hcp[:nc].view(torch.int32).view(-1, 4)[:, 0].numpy().astype(np.int64)
+    assert np.array_equal(f32(state).view(np.uint32), f32(st_h).view(np.uint32))
+    assert np.array_equal(f32(out)[rows].view(np.uint32), f32(out_h)[rows].view(np.uint32))
+    np.testing.assert_array_equal(u8(cache), u8(cache_h))
+    ref = _expect(ora, cache0, ps, f32(out)[rows], cache_loc.numpy()[rows], True)
+    np.testing.assert_array_equal(u8(cache), ref)
