@@ -79,8 +79,8 @@ struct Layout {
   static constexpr int kApe = kSc + kSt * kBoxBytes;                  // [128][kCh] fp32 * log2(e)
   static constexpr int kPart = kApe + 128 * kCh * 4;                  // [2][kCWarps][3][kCh] fp32
   static constexpr int kRow = kPart + 2 * kCWarps * 3 * kCh * 4;     // FP8 stage: [2][kCh] fp32
-  static constexpr int kBar = kRow + (kFp8 ? 2 * kCh * 4 : 0);       // full, empty, ready (, rowready, rowfree)
-  static constexpr int kBytes = kBar + (2 * kSt + 2 + (kFp8 ? 4 : 0)) * 8;
+  static constexpr int kBar = kRow + (kFp8 ? 2 * kCh * 4 : 0);       // full, empty, ready (, rowready)
+  static constexpr int kBytes = kBar + (2 * kSt + 2 + (kFp8 ? 2 : 0)) * 8;
   static_assert(kRows == kCWarps * kRowsPerWarp, "each consumer warp owns 8 rows of a stage");
 };
 
@@ -160,7 +160,6 @@ __global__ void __launch_bounds__(Layout<InT, kFp8>::kThreads, 1)
   uint64_t* empty = full + kSt;
   uint64_t* ready = empty + kSt;
   uint64_t* rowready = ready + 2;  // FP8 stage only: a segment's row is staged
-  uint64_t* rowfree = ready + 4;   // FP8 stage only: the FP8 warp has read it
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slice = blockIdx.x % S;
@@ -171,13 +170,13 @@ __global__ void __launch_bounds__(Layout<InT, kFp8>::kThreads, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kCWarps);
     }
-    mbar_init(&ready[0], kCWarps);
-    mbar_init(&ready[1], kCWarps);
+    // with the FP8 stage the FP8 warp also arrives on `ready`: its arrival for
+    // a segment means it has read the row buffer that segment will reuse
+    mbar_init(&ready[0], kCWarps + (kFp8 ? 1 : 0));
+    mbar_init(&ready[1], kCWarps + (kFp8 ? 1 : 0));
     if constexpr (kFp8) {
       mbar_init(&rowready[0], kCh / 32);
       mbar_init(&rowready[1], kCh / 32);
-      mbar_init(&rowfree[0], 1);
-      mbar_init(&rowfree[1], 1);
     }
     fence_mbar_init();
   }
@@ -227,8 +226,14 @@ __global__ void __launch_bounds__(Layout<InT, kFp8>::kThreads, 1)
     if (warp == kCWarps + 1) {
       // ---------------------------------------------------------- FP8 warp
       // takes each segment's staged row (block `slice` of the output row) and
-      // stores it through the pooled output stage, while the consumers go on
+      // stores it through the pooled output stage, while the consumers go on;
+      // the consumers reuse a row buffer only after passing a `ready` barrier
+      // that the FP8 warp joins once it has read that buffer
       pdl_trigger();
+      if (lane == 0) {  // the first use of each row buffer needs no read to wait for
+        mbar_arrive(&ready[0]);
+        mbar_arrive(&ready[1]);
+      }
       uint32_t it = 0;
       uint4 next = load_plan(a.compress_plan, group, n);
       for (uint32_t p = group; p < n; p += ngroups) {
@@ -251,7 +256,7 @@ __global__ void __launch_bounds__(Layout<InT, kFp8>::kThreads, 1)
         }
         const float4 v = reinterpret_cast<const float4*>(smem + L::kRow + buf * kCh * 4)[lane];
         __syncwarp();
-        if (lane == 0) mbar_arrive(&rowfree[buf]);
+        if (lane == 0) mbar_arrive(&ready[buf]);  // counts toward the segment two ahead
         if (!slot_ok) continue;
         if (loc < 0 || loc >= a.num_pages * a.page_size) {
           if (lane == 0 && slice == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
@@ -409,15 +414,6 @@ __global__ void __launch_bounds__(Layout<InT, kFp8>::kThreads, 1)
       return;
     }
     ++it;
-    if constexpr (kFp8) {
-      // the row buffer of this parity was last used two segments ago: wait
-      // until the FP8 warp has read it
-      const uint32_t use = (it - 1) >> 1;  // this segment's use of buffer `buf`
-      if (cw < kCh / 32 && use > 0 && !mbar_wait(&rowfree[buf], (use - 1) & 1)) {
-        if (lane == 0) flag_error(a.err, CKV_DEVERR_TIMEOUT);
-        return;
-      }
-    }
     if (t < kCh && slot_ok) {
       float m = kNegBig;
 #pragma unroll
