@@ -60,6 +60,12 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinBlocks)
   // The slot index gates the dependent state loads: issue it before the input stream.
   const int32_t index = in_batch ? a.indices[b] : 0;
   const int32_t seq_len = in_batch ? a.seq_lens[b] : 1;
+  // the FP8 stage's cache row, fetched with the other per-request words so that
+  // its latency is not paid at the stage's barrier
+  int64_t cache_loc = kNoRow;
+  if constexpr (kFp8) {
+    if (in_batch && t == 0) cache_loc = a.cache_loc[b];
+  }
   const int col = 4 * t;
   const InT* in = static_cast<const InT*>(a.input) + static_cast<int64_t>(in_batch ? b : 0) * 2 * D;
   float4 kin[G], sin_[G];
@@ -148,7 +154,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinBlocks)
 #pragma unroll
       for (int g = 0; g < G; ++g) *reinterpret_cast<float4*>(&s_row[r][col + kSpan * g]) = nkv[g];
     }
-    if (t == 0) s_loc[r] = closing ? a.cache_loc[b] : kNoRow;
+    if (t == 0) s_loc[r] = closing ? cache_loc : kNoRow;
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t rows = a.num_pages * a.page_size;
