@@ -6,10 +6,11 @@
 // with kv normalised; input row: [2D] = kv | score.
 //
 // Design for sm_103a (memory bound, SIMT, no tensor cores):
-//   decode  -- one thread per 4 channels (D / 4 threads per request, the
-//              whole batch resident in one wave); the input row is issued
+//   decode  -- two 4-channel groups per thread (D / 8 threads per request,
+//              the whole batch resident in one wave); the input row is issued
 //              before the slot index is known, the slot state is skipped at
-//              chunk position 0; two ex2 per channel.
+//              chunk position 0, unchanged 32-byte sectors of the running max
+//              are not rewritten; two ex2 per channel.
 //   prefill -- one CTA of 8 warps per (segment, 128-channel slice).  Warp w
 //              owns chunk positions [16w, 16w+16), loads them 8 tokens at a
 //              time (16-byte fp32 / 8-byte bf16 vectors, streaming hints) and
@@ -19,6 +20,10 @@
 //              segment starts mid-chunk, then stored.  Compress and write
 //              passes are two launches in stream order (optionally chained
 //              by programmatic dependent launch).
+//   FP8 stage (the _fp8 calls; kFp8 instantiations) -- each emitted row is
+//              staged in shared memory and stored, 128-channel block by
+//              block, through the pooled path's rotation and quantisation
+//              (ckv_fp8.cuh) into a paged FP8 cache.
 #include <type_traits>
 
 #include "ckv_device.cuh"

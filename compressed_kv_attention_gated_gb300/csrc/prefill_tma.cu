@@ -24,6 +24,10 @@
 //     running (max, sum, weighted sum) per channel; at the end of a segment the
 //     eight partials meet in shared memory (double-buffered, mbarrier
 //     synchronised), are merged with the prefetched prior state and stored.
+//   * with the FP8 stage (kFp8) one more warp takes each segment's staged row
+//     slice through the pooled path's rotation and quantisation into the
+//     paged FP8 cache, joining the segment barrier two segments ahead once it
+//     has read a row buffer, so the consumers never wait for it;
 //   * every wait is bounded (two seconds of wall time); a timeout sets
 //     CKV_DEVERR_TIMEOUT in the error word and the thread leaves; the producer
 //     drains its own outstanding TMA loads before it exits.
