@@ -319,3 +319,35 @@ def test_c128_prefill_sentinels_and_bad_plans(variant, ck):
     torch.cuda.synchronize()
     assert int(err.item()) == 0x8
     assert np.all(f32(out) == CANARY)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_c128_prefill_masked_rows_do_not_leak(variant, ck, ora, dtype):
+    """Rows outside a segment carry weight 0 (sglang page: padded kv is zeroed so
+    that 0 * NaN never happens).  One request's input rows are NaN and +inf; the
+    TMA boxes and token batches of its neighbours overlap them, yet every other
+    request's rows and states must equal the oracle's."""
+    from compressed_kv_attention_gated_gb300 import synth
+
+    d = synth.c128_prefill("cpu", seed=23, B=10, D=256, max_prefix=300, max_extend=90, dtype=dtype)
+    ext = d["extend_lens"].numpy()
+    starts = np.concatenate([[0], np.cumsum(ext)[:-1]])
+    bad = 4
+    x = d["input"].clone()
+    x[starts[bad]:starts[bad] + ext[bad], :d["D"]] = float("nan")
+    x[starts[bad]:starts[bad] + ext[bad], d["D"]:] = float("inf")
+    d["input"] = x
+    g_state, g_out, err, (cp, wp, nc, nw) = _prefill_gpu(ck, d)
+    assert err == 0
+    idx = d["indices"].numpy()
+    ref_out, written, fs, sw = ora.c128_prefill(f32(d["state"]), _np_input(x), f32(d["ape"]), idx,
+                                                d["seq_lens"].numpy(), d["extend_lens"].numpy())
+    owner = np.repeat(np.arange(len(ext)), ext)
+    rows = written & (owner != bad)
+    assert rows.sum() > 0
+    assert_close_rel(f32(g_out)[rows], ref_out[rows], "rows of clean requests")
+    keep = sw & (np.arange(len(ext)) != bad)
+    gs = f32(g_state)
+    assert_close_abs(gs[idx[keep], 0], fs[keep, 0], what="max")
+    assert_close_rel(gs[idx[keep], 1], fs[keep, 1], "sum")
+    assert_close_rel(gs[idx[keep], 2], fs[keep, 2], "kv")
