@@ -202,10 +202,21 @@ class Step:
         self._accounting()
 
     # -- calls -------------------------------------------------------------
+    nvtx = False  # --nvtx: an NVTX range named after the C entry point around each call
+
     def call(self, i, pdl=False):
         """Call i of the step; with pdl every launch is a programmatic dependent
         launch on its predecessor (each kernel still waits for it on the device
         before touching memory, but its launch overlaps the predecessor's tail)."""
+        if self.nvtx:
+            torch.cuda.nvtx.range_push(self.names[i])
+            try:
+                return self._call(i, pdl)
+            finally:
+                torch.cuda.nvtx.range_pop()
+        return self._call(i, pdl)
+
+    def _call(self, i, pdl):
         ck, pd, cd, cp, lc = self.ck, self.pd, self.cd, self.cp, self.lc
         if i == 0:
             ck.ckv_kpool_decode_update(pd["kv_cache"], pd["ring"], pd["tail_slot_mapping"], pd["slot_mapping"],
@@ -841,6 +852,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--nvtx", action="store_true",
+                    help="NVTX range around each call (e.g. ncu --nvtx --nvtx-include 'c128_online_decode/')")
     ap.add_argument("--no-decode-cold", action="store_true",
                     help="skip the L2-cold CUDA-graph timing of the two decode calls")
     ap.add_argument("--no-pdl", action="store_true", help="plain stream order between the five calls")
@@ -876,6 +889,7 @@ def main():
 
     libbuild.build()
     step = Step(dev, seed=replica_seed(rank))
+    step.nvtx = args.nvtx
     nk = len(step.names)
     stream = torch.cuda.Stream(dev)
     torch.cuda.synchronize()
