@@ -220,6 +220,11 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
   }
   const int chunk_offset = static_cast<int>(pic + 1 - window);
   const int window_end = static_cast<int>(pic + 1);
+  // the FP8 stage's cache row, fetched now so that the CTA does not end on its latency
+  int64_t fp8_loc = 0;
+  if constexpr (kFp8) {
+    if (threadIdx.x < 32) fp8_loc = a.cache_loc[ragged_id];
+  }
   int32_t load_index = -1, store_index = -1;
   if (chunk_offset != 0) load_index = a.load_indices[batch];
   if (kWrite) store_index = a.indices[batch];
@@ -325,7 +330,7 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
       s_row[t] = kv;
       asm volatile("bar.sync 1, 128;" ::: "memory");  // the 128 epilogue threads
       if (t < 32) {
-        const int64_t loc = a.cache_loc[ragged_id];
+        const int64_t loc = fp8_loc;
         if (loc < 0 || loc >= a.num_pages * a.page_size) {
           if (t == 0 && slice == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
         } else {
