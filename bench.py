@@ -54,9 +54,8 @@ WORKLOAD = ("serving step: pooled decode/verify B=512 N=4 P=16 D=128 + c128 deco
 
 # DRAM traffic (read + write bytes) per launch of the dominant kernel from one
 # ncu capture of a 131,072-token case, scaled by tokens to the 8 x 131,072-token
-# launch (profiles/c128_prefill_tma_kernel_bf16_d512_131072tok.md); `src` is a
-# hash of the kernel's source files at capture time: any later change to them
-# turns the figure into null.
+# launch; `src` is a hash of the kernel's source files at capture time: any
+# later change to them turns the figure into null.
 NCU_TRAFFIC = {
     "c128_online_prefill_bf16": {"bytes_per_launch": 2172.4e6, "files": ["prefill_tma.cu", "ckv_tma.cuh", "ckv_fp8.cuh",
                                                                          "ckv_device.cuh"],

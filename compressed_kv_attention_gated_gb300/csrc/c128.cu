@@ -187,6 +187,7 @@ template <int D, typename InT, bool kWrite, bool kFp8>
 __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
     c128_prefill_kernel(const __grid_constant__ C128PrefillArgs a) {
   static_assert(!(kWrite && kFp8), "the FP8 output stage belongs to the compress pass");
+  static_assert(kPrefillWarps * 32 >= 128, "the epilogue's 128 threads own one channel of the slice each");
   constexpr int S = D / 128;  // 128-channel slices per row
   __shared__ __align__(16) float4 s_m[kPrefillWarps][32];
   __shared__ __align__(16) float4 s_s[kPrefillWarps][32];

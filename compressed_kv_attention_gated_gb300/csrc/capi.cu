@@ -472,7 +472,7 @@ ckv_status ckv_check_distinct_noalloc(const void* ids, int32_t id_bytes, int64_t
   if ((id_bytes != 4 && id_bytes != 8) || n < 0 || range < 1) return CKV_ERR_SHAPE;
   if (range > ckv::noalloc_check_max_range()) return CKV_ERR_SHAPE;  // beyond the fixed bitmap
   if (!err_word || (n > 0 && !ids)) return CKV_ERR_NULL;
-  if (!aligned(ids, static_cast<uintptr_t>(id_bytes))) return CKV_ERR_ALIGN;
+  if (!aligned(ids, static_cast<uintptr_t>(id_bytes)) || !aligned(err_word, 4)) return CKV_ERR_ALIGN;
   return cuda_status(ckv::launch_check_distinct_noalloc(ids, id_bytes, n, range, err_word,
                                                         static_cast<cudaStream_t>(stream)));
 }

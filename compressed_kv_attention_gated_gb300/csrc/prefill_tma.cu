@@ -85,6 +85,9 @@ struct Layout {
   static constexpr int kRow = kPart + 2 * kCWarps * 3 * kCh * 4;     // FP8 stage: [2][kCh] fp32
   static constexpr int kBar = kRow + (kFp8 ? 2 * kCh * 4 : 0);       // full, empty, ready (, rowready)
   static constexpr int kBytes = kBar + (2 * kSt + 2 + (kFp8 ? 2 : 0)) * 8;
+  // the FP8 warp reads one float4 per lane (128 channels) and stores it as one
+  // 128-channel FP8 block per slice
+  static_assert(!kFp8 || kCh == 128, "the FP8 warp stores one 128-channel block per slice");
   static_assert(kRows == kCWarps * kRowsPerWarp, "each consumer warp owns 8 rows of a stage");
 };
 

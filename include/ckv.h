@@ -417,8 +417,11 @@ ckv_status ckv_check_distinct(const void* ids, int32_t id_bytes, int64_t n, int6
  *              CKV_ERR_SHAPE and launches nothing
  * The first call on each device looks up the array's device address (with
  * that device current) and keeps it; make that first call before any stream
- * capture.  Every call uses the same array: it is cleared at the start of each
- * call, and calls that overlap on the GPU (other streams, other threads) race.
+ * capture.  The kept address belongs to the device's context of that moment:
+ * do not reset the device (cudaDeviceReset) after the first call in a process
+ * that calls this again.  Every call uses the same array: it is cleared at the
+ * start of each call, and calls that overlap on the GPU (other streams, other
+ * threads) race.
  */
 #define CKV_NOALLOC_MAX_RANGE (1 << 21)
 ckv_status ckv_check_distinct_noalloc(const void* ids, int32_t id_bytes, int64_t n, int64_t range,

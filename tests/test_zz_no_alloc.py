@@ -19,8 +19,8 @@ MAX_RANGE = 1 << 21
 
 
 def test_noalloc_rejects_range_beyond_its_bitmap():
-    """CPU: a range above 2^21 ids (and a missing error word) is refused during
-    argument checking, before anything is launched."""
+    """CPU: a range above 2^21 ids, a missing or misaligned error word are
+    refused during argument checking, before anything is launched."""
     from compressed_kv_attention_gated_gb300 import build, ckv
 
     build.build()
@@ -29,6 +29,8 @@ def test_noalloc_rejects_range_beyond_its_bitmap():
     assert L.ckv_check_distinct_noalloc(one, 4, 10, MAX_RANGE + 1, one, None) == 2
     assert L.ckv_check_distinct_noalloc(one, 4, 10, MAX_RANGE, None, None) == 1
     assert L.ckv_check_distinct_noalloc(one, 3, 10, 64, one, None) == 2
+    # a misaligned error word is refused like in every other entry point
+    assert L.ckv_check_distinct_noalloc(one, 4, 10, 64, ctypes.c_void_p(18), None) == 4
 
 
 @pytest.fixture(scope="module")
