@@ -35,11 +35,18 @@ def test_bf16_matches_torch_cast_on_fp32(ora):
         # exact ties between two bf16 neighbours (low 16 bits = 0x8000)
         (rng.integers(0x0080, 0x7F00, 2000, dtype=np.uint32) << 16 | 0x8000).view(np.float32),
         np.array([0.0, -0.0, 1e-40, -1e-40, 3.0e38, 1.17e-38], np.float32),
+        # around the largest bf16 value (2 - 2^-7) * 2^127: below the midpoint to
+        # 2^128 it stays finite, from the midpoint on it rounds to infinity
+        np.array([3.3895e38, 3.3960e38, 3.3962e38, 3.4e38, -3.4e38], np.float32),
     ])
     vals = vals[np.isfinite(vals)]
     ref = _bf16_bits(vals)
     got = np.array([ora.bf16_from_double(float(v)) for v in vals], np.uint16)
     np.testing.assert_array_equal(got, ref)
+    assert ora.bf16_from_double(3.4e38) == 0x7F80 and ora.bf16_from_double(-3.4e38) == 0xFF80
+    assert ora.bf16_from_double(float(np.ldexp(255.0, 120))) == 0x7F7F  # the largest finite value itself
+    h = ora.bf16_from_double(float("nan"))
+    assert (h & 0x7F80) == 0x7F80 and (h & 0x007F) != 0  # a NaN pattern
 
 
 def test_bf16_from_double_is_nearest(ora):
@@ -329,6 +336,26 @@ def test_kpool_compress_cache_layout(ora):
         assert np.all(flat[mask] == 0xAB)
 
 
+def test_kpool_compress_codes_without_cache_write(ora):
+    """write_cache off: the cache is untouched and the returned codes and
+    scales are those a cache write would have stored."""
+    rng = np.random.default_rng(43)
+    P, D, ps, n = 16, 128, 8, 5
+    k = _rand_bf16(rng, (n, P, D))
+    s = _rand_bf16(rng, (n, P, D))
+    ape = (rng.standard_normal((P, D)) * 0.1).astype(np.float32)
+    loc = np.arange(n, dtype=np.int64)
+    c0 = np.full((1, ps, D + 4), 0x3C, np.uint8)
+    r = ora.kpool_compress(c0, ps, k, s, ape, loc, write_cache=False, return_compressed=True)
+    assert np.all(c0 == 0x3C)
+    c1 = np.full((1, ps, D + 4), 0x3C, np.uint8)
+    ora.kpool_compress(c1, ps, k, s, ape, loc)
+    flat = c1.reshape(-1)
+    for i in range(n):
+        np.testing.assert_array_equal(flat[i * D:(i + 1) * D], r["q"][i])
+        assert flat[ps * D + 4 * i:ps * D + 4 * i + 4].view(np.float32)[0] == r["scale"][i]
+
+
 def test_kpool_compress_write_mask(ora):
     rng = np.random.default_rng(14)
     P, D, ps = 16, 128, 64
@@ -415,6 +442,60 @@ def test_kpool_decode_padding_is_inert(ora):
     assert np.all(cache == 0)
 
 
+_KD_GOLDEN = json.load(open(os.path.join(GOLDEN, "kpool_decode_examples.json")))
+
+
+def kpool_decode_golden_inputs(fx, D=128):
+    """Arrays of the pooled-decode fixture: one token per request."""
+    P = fx["P"]
+    ring = np.zeros((2, 2, P, D), np.float32)
+    ring[:, 0] = np.array(fx["ring"]["key"], np.float32)[:, :, None]
+    ring[:, 1] = np.array(fx["ring"]["score"], np.float32)[:, :, None]
+    toks = fx["tokens"]
+    col = lambda name: np.array([[t[name]] for t in toks], np.int32)
+    key = np.array([[np.full(D, t["key"])] for t in toks], np.float32)
+    score = np.array([[np.full(D, t["score"])] for t in toks], np.float32)
+    ape = np.repeat(np.array(fx["ape"], np.float32)[:, None], D, 1)
+    cache = np.full((fx["pages"], fx["page_size"], D + 4), fx["canary"], np.uint8)
+    return {"ring": _bf16_bits(ring), "tail_slot_mapping": col("tail_slot"), "slot_mapping": col("slot_mapping"),
+            "positions": col("position"), "key": _bf16_bits(key), "score": _bf16_bits(score), "ape": ape,
+            "cache": cache}
+
+
+def kpool_decode_golden_check(fx, cache, ring, D=128):
+    """The cache and ring after the fixture's call, against the hand-derived values."""
+    P, ps = fx["P"], fx["page_size"]
+    e = fx["expect"]
+    flat = cache.reshape(-1)
+    page, tok = divmod(e["cache"]["loc"], ps)
+    row0 = page * ps * (D + 4) + tok * D
+    sc0 = page * ps * (D + 4) + ps * D + 4 * tok
+    assert flat[row0] == e["cache"]["q0"]
+    assert np.all(flat[row0 + 1:row0 + D] == e["cache"]["q_rest"])
+    assert flat[sc0:sc0 + 4].view(np.float32)[0] == e["cache"]["scale"]
+    rest = np.ones(flat.size, bool)
+    rest[row0:row0 + D] = False
+    rest[sc0:sc0 + 4] = False
+    assert np.all(flat[rest] == fx["canary"]), "only the closing row's bytes change"
+    want = np.zeros((2, 2, P, D), np.float32)
+    want[:, 0] = np.array(e["ring_key"], np.float32)[:, :, None]
+    want[:, 1] = np.array(e["ring_score"], np.float32)[:, :, None]
+    np.testing.assert_array_equal(ring, _bf16_bits(want))
+
+
+def test_kpool_decode_golden_gating_and_block_clamp(ora):
+    """Hand-derived: a closing token whose tail slot is negative still closes
+    its pool, from ring block 0 (block = max(tail_slot, 0) // P), and stashes
+    nothing; a token at the closing slot without a cache location only stashes;
+    an open slot with a negative tail slot changes nothing."""
+    fx = _KD_GOLDEN
+    a = kpool_decode_golden_inputs(fx)
+    ring, cache = a["ring"].copy(), a["cache"].copy()
+    ora.kpool_decode_update(cache, fx["page_size"], ring, a["tail_slot_mapping"], a["slot_mapping"],
+                            a["positions"], a["key"], a["score"], a["ape"], round_scale=True)
+    kpool_decode_golden_check(fx, cache, ring)
+
+
 def test_kpool_seed_tail_selects_last_pool(ora):
     # two requests of 21 and 7 prefill tokens; request r's tail block is r; a token is
     # seeded iff it is among its request's last P tokens
@@ -439,16 +520,180 @@ def test_kpool_seed_tail_selects_last_pool(ora):
 
 
 # ---------------------------------------------------------------- online c128
-def test_c128_golden_two_tokens(ora):
-    case = json.load(open(os.path.join(GOLDEN, "c128_examples.json")))["cases"][0]
+_C128_GOLDEN = json.load(open(os.path.join(GOLDEN, "c128_examples.json")))["cases"]
+
+
+@pytest.mark.parametrize("case", [c for c in _C128_GOLDEN if "state_after" in c], ids=lambda c: c["name"])
+def test_c128_golden_two_tokens(ora, case):
+    """fp32 and bf16 input rows (the bf16 case pins the oracle's bf16 branch)."""
     D = 128
     state = np.zeros((1, 3, D), np.float32)
     ape = np.zeros((128, D), np.float32)
     for t, (kk, ss) in enumerate(zip(case["keys"], case["scores"])):
         inp = np.concatenate([np.full(D, kk, np.float32), np.full(D, ss, np.float32)])[None]
+        if case["dtype"] == "bf16":
+            inp = _bf16_bits(inp)
         out, ns, closed = ora.c128_decode(state, inp, ape, np.array([0]), np.array([t + 1]))
         np.testing.assert_allclose(ns[0, :, 0], case["state_after"][t], rtol=1e-6, atol=1e-6)
+        assert np.all(ns[0] == ns[0, :, :1])  # every channel alike
         state[0] = ns[0].astype(np.float32)
+
+
+def test_c128_golden_equal_logits_full_chunk(ora):
+    """Keys 0..127 under equal logits: after 127 tokens the state is (c, 127,
+    63); the 128th token closes the chunk with the mean 63.5.  The same chunk
+    as one prefill segment emits the same row.  Both input types."""
+    case = next(c for c in _C128_GOLDEN if "closing_kv" in c)
+    D = 128
+    keys = np.arange(128, dtype=np.float32)
+    for dtype in ("f32", "bf16"):
+        for logit in (0.0, -3.5):
+            ape = np.zeros((128, D), np.float32)
+            state = np.zeros((1, 3, D), np.float32)
+            for t in range(128):
+                inp = np.concatenate([np.full(D, keys[t], np.float32), np.full(D, logit, np.float32)])[None]
+                if dtype == "bf16":
+                    inp = _bf16_bits(inp)
+                out, ns, closed = ora.c128_decode(state, inp, ape, np.array([0]), np.array([128 * 3 + t + 1]))
+                assert closed[0] == (t == 127)
+                if t == 126:
+                    np.testing.assert_allclose(ns[0, :, 0], [logit, 127.0, 63.0], rtol=1e-12, atol=1e-12)
+                if t < 127:
+                    state[0] = ns[0].astype(np.float32)
+            np.testing.assert_allclose(out[0], case["closing_kv"], rtol=0, atol=1e-12)
+            chunk = np.concatenate([np.repeat(keys[:, None], D, 1), np.full((128, D), logit, np.float32)], 1)
+            if dtype == "bf16":
+                chunk = _bf16_bits(chunk)
+            pout, w, _, sw = ora.c128_prefill(np.zeros((1, 3, D), np.float32), chunk, ape, np.array([0]),
+                                              np.array([128]), np.array([128]))
+            assert w[127] and w.sum() == 1 and not sw[0]
+            np.testing.assert_allclose(pout[127], case["closing_kv"], rtol=0, atol=1e-12)
+
+
+def _two_pass(k, z):
+    """Softmax-weighted mean of rows k under logits z (both [n, D]), computed
+    straight from the definition in double: (max, sum, kv)."""
+    k = np.asarray(k, np.float64)
+    z = np.asarray(z, np.float64)
+    m = z.max(0)
+    w = np.exp(z - m)
+    return m, w.sum(0), (w * k).sum(0) / w.sum(0)
+
+
+def test_c128_decode_merge_equals_two_pass_over_prior_tokens(ora):
+    """A slot whose state is the two-pass (max, sum, kv) of p virtual tokens at
+    chunk positions 0..p-1 (built here in numpy), updated with one token at
+    position p, equals the two-pass over all p+1 tokens; at p = 127 the emitted
+    row does and the slot is left alone.  Pins the merge branch of the decode."""
+    rng = np.random.default_rng(40)
+    D = 128
+    ps = [1, 2, 17, 63, 64, 100, 126, 127]
+    B = len(ps)
+    ape = (rng.standard_normal((128, D)) * 0.1).astype(np.float32)
+    k = rng.standard_normal((B, 128, D)).astype(np.float32)
+    s = (rng.standard_normal((B, 128, D)) * 2).astype(np.float32)
+    z = s.astype(np.float64) + ape
+    state = np.zeros((2 * B, 3, D), np.float32)
+    slots = rng.permutation(2 * B)[:B]
+    for b, p in enumerate(ps):
+        m, sm, kv = _two_pass(k[b, :p], z[b, :p])
+        state[slots[b]] = np.stack([m, sm, kv]).astype(np.float32)
+    inp = np.stack([np.concatenate([k[b, p], s[b, p]]) for b, p in enumerate(ps)])
+    seq = np.array([128 * (b + 2) + p + 1 for b, p in enumerate(ps)])
+    out, ns, closed = ora.c128_decode(state, inp, ape, slots.astype(np.int32), seq)
+    for b, p in enumerate(ps):
+        # the stored state is fp32: compare with the two-pass over the fp32-rounded prior
+        m, sm, kv = _two_pass(k[b, :p + 1], z[b, :p + 1])
+        assert closed[b] == (p == 127)
+        np.testing.assert_allclose(ns[b, 2], kv, rtol=1e-6, atol=1e-6)
+        np.testing.assert_allclose(ns[b, 0], m, rtol=0, atol=1e-6)
+        # the sum is relative to the running max: equal up to the fp32 rounding of the prior state
+        np.testing.assert_allclose(ns[b, 1], sm, rtol=1e-6)
+        if p == 127:
+            np.testing.assert_allclose(out[b], kv, rtol=1e-6, atol=1e-6)
+
+
+def test_c128_prefill_merge_equals_two_pass_over_prior_tokens(ora):
+    """Prefill of a request whose first extend token sits mid-chunk: the slot
+    holds the two-pass (max, sum, kv) of the chunk's p earlier (virtual) tokens,
+    built here in numpy.  The closing row of that chunk must equal the two-pass
+    over all 128 of its tokens, later chunks the two-pass over their own
+    tokens, and the trailing partial chunk's new state the two-pass over its
+    tokens (merged with the prior when the extend ends in the first chunk).
+    Pins the prefill's merge with a stored partial directly."""
+    rng = np.random.default_rng(41)
+    D = 128
+    cases = [(37, 91), (37, 400), (5, 20), (127, 1), (127, 130), (64, 64), (1, 300)]  # (p, extend)
+    B = len(cases)
+    ape = (rng.standard_normal((128, D)) * 0.1).astype(np.float32)
+    chunk0 = 128 * np.arange(1, B + 1)  # request b's prior chunk starts at position chunk0[b]
+    state = np.zeros((2 * B, 3, D), np.float32)
+    load = rng.permutation(2 * B)[:B].astype(np.int32)
+    toks_k, toks_s, rows = [], [], []
+    seq, ext = [], []
+    for b, (p, e) in enumerate(cases):
+        n = p + e
+        k = rng.standard_normal((n, D)).astype(np.float32)
+        s = (rng.standard_normal((n, D)) * 2).astype(np.float32)
+        m, sm, kv = _two_pass(k[:p], s[:p].astype(np.float64) + ape[:p])
+        state[load[b]] = np.stack([m, sm, kv]).astype(np.float32)
+        toks_k.append(k)
+        toks_s.append(s)
+        rows.append(np.concatenate([k[p:], s[p:]], 1))
+        seq.append(chunk0[b] + n)
+        ext.append(e)
+    inp = np.concatenate(rows, 0)
+    out, written, fs, sw = ora.c128_prefill(state, inp, ape, load, np.array(seq), np.array(ext))
+    base = 0
+    for b, (p, e) in enumerate(cases):
+        n = p + e
+        k, s = toks_k[b], toks_s[b]
+        z = s.astype(np.float64) + ape[np.arange(n) % 128]
+        # chunks of this request in local token numbering (local 0 = chunk position 0)
+        for c0 in range(0, n, 128):
+            c1 = min(n, c0 + 128)
+            m, sm, kv = _two_pass(k[c0:c1], z[c0:c1])
+            if c1 - c0 == 128:
+                r = base + (c1 - 1 - p)  # ragged row of the closing token
+                assert written[r]
+                np.testing.assert_allclose(out[r], kv, rtol=1e-6, atol=1e-6)
+            else:
+                assert sw[b]
+                np.testing.assert_allclose(fs[b, 2], kv, rtol=1e-6, atol=1e-6)
+                np.testing.assert_allclose(fs[b, 0], m, rtol=0, atol=1e-6)
+                np.testing.assert_allclose(fs[b, 1], sm, rtol=1e-6)
+        if n % 128 == 0:
+            assert not sw[b]
+        assert written[base:base + e].sum() == n // 128
+        base += e
+
+
+@pytest.mark.parametrize("fn", ["decode", "prefill"])
+def test_c128_bf16_input_equals_widened_fp32(ora, fn):
+    """The bf16 input branch reads each value as its exact fp32 widening: the
+    same rows given as bf16 bits and as fp32 give identical results."""
+    rng = np.random.default_rng(42)
+    D = 256
+    ape = (rng.standard_normal((128, D)) * 0.1).astype(np.float32)
+    state = rng.standard_normal((64, 3, D)).astype(np.float32)
+    state[:, 1] = np.abs(state[:, 1]) + 1
+    if fn == "decode":
+        B = 40
+        bits = _bf16_bits(rng.standard_normal((B, 2 * D)).astype(np.float32) * 3)
+        idx = rng.permutation(64)[:B].astype(np.int32)
+        seq = rng.integers(1, 5000, B)
+        seq[:3] = [1, 128, 129]
+        r_b = ora.c128_decode(state, bits, ape, idx, seq)
+        r_f = ora.c128_decode(state, _bf16_round_bits(bits), ape, idx, seq)
+    else:
+        ext = np.array([300, 5, 128, 77])
+        seq = ext + np.array([0, 60, 128, 200])
+        bits = _bf16_bits(rng.standard_normal((int(ext.sum()), 2 * D)).astype(np.float32) * 3)
+        idx = rng.permutation(64)[:4].astype(np.int32)
+        r_b = ora.c128_prefill(state, bits, ape, idx, seq, ext)
+        r_f = ora.c128_prefill(state, _bf16_round_bits(bits), ape, idx, seq, ext)
+    for a, b in zip(r_b, r_f):
+        np.testing.assert_array_equal(np.nan_to_num(a, nan=7.0), np.nan_to_num(b, nan=7.0))
 
 
 def test_c128_decode_chunk_equals_two_pass(ora):
@@ -637,6 +882,10 @@ def test_c128_rows_to_cache_golden(ora, round_scale):
     np.testing.assert_array_equal(cache, expect)
     if not round_scale:
         assert np.all(cache[1].reshape(-1)[D:2 * D] == 0x7E)  # 448, the largest e4m3 value
+    # a row with a negative location is skipped: nothing changes
+    before = cache.copy()
+    ora.c128_rows_to_cache(cache, ps, row * 3, np.array([-1]), round_scale=round_scale)
+    np.testing.assert_array_equal(cache, before)
 
 
 @pytest.mark.parametrize("round_scale", [False, True])
