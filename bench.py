@@ -202,6 +202,7 @@ class Step:
 
     # -- calls -------------------------------------------------------------
     nvtx = False  # --nvtx: an NVTX range named after the C entry point around each call
+    round_scale = True  # FP8 scale of the pooled decode call: power of two, or linear when False
 
     def call(self, i, pdl=False):
         """Call i of the step; with pdl every launch is a programmatic dependent
@@ -219,8 +220,8 @@ class Step:
         ck, pd, cd, cp, lc = self.ck, self.pd, self.cd, self.cp, self.lc
         if i == 0:
             ck.ckv_kpool_decode_update(pd["kv_cache"], pd["ring"], pd["tail_slot_mapping"], pd["slot_mapping"],
-                                       pd["positions"], pd["key"], pd["score"], pd["ape"], round_scale=True,
-                                       use_pdl=pdl, err_word=self.err)
+                                       pd["positions"], pd["key"], pd["score"], pd["ape"],
+                                       round_scale=self.round_scale, use_pdl=pdl, err_word=self.err)
         elif i == 1:
             ck.ckv_c128_online_decode(cd["state"], cd["input"], cd["out"], cd["ape"], cd["indices"], cd["seq_lens"],
                                       use_pdl=pdl, err_word=self.err)
@@ -732,11 +733,12 @@ def run_case(args):
 
 
 def run_rotation(args):
-    """--case c128_decode|kpool_decode --rotate: print rotation_timings() as one JSON line."""
-    print(json.dumps(rotation_timings(args.case, args.steps, args.warmup)))
+    """--case c128_decode|kpool_decode|latency_floor0|1|2 --rotate: print
+    rotation_timings() as one JSON line."""
+    print(json.dumps(rotation_timings(args.case, args.steps, args.warmup, round_scale=not args.linear_scale)))
 
 
-def rotation_timings(case, replays=100, warmup=20):
+def rotation_timings(case, replays=100, warmup=20, round_scale=True):
     """Decode calls timed L2-cold and warm, each replayed from one CUDA graph.
 
     Cold: R independent instances of the batch (R x algorithmic bytes >= 4 x
@@ -744,9 +746,24 @@ def rotation_timings(case, replays=100, warmup=20):
     replay is bracketed by events and the median replay time / R is the time of
     one call that finds none of its data in L2.  Warm: a graph of one call on
     one instance (its data L2-resident after the first replay).  Both with and
-    without programmatic dependent launch between the captured calls.  The
-    pooled instances share one cache tensor, each writing its own rows
-    (location r * B + b for request b of instance r)."""
+    without programmatic dependent launch between the captured calls.
+
+    c128 decode: before every replay (outside the events) each instance's
+    state pool is restored from a pristine copy and a buffer of twice the L2
+    size is written, so every timed call updates states it has never seen:
+    its running max moves at the workload's own rate instead of never (a
+    replay into states it already updated leaves every max unchanged).  The
+    bytes it physically writes (the max-row sectors it leaves alone excluded)
+    are reported beside the algorithmic bytes.
+
+    Pooled decode: the instances share one cache tensor, each writing its own
+    rows (location r * B + b for request b of instance r); round_scale picks
+    the power-of-two or the linear FP8 scale.
+
+    latency_floor: the ckv_latency_probe kernels (0, 1 and 2 dependent global
+    round trips per warp) in the pooled decode's launch shape, R instances of
+    512 warps with an L2 flush before every replay: the floor under the pooled
+    decode's cold time."""
     import math
 
     import compressed_kv_attention_gated_gb300 as ck
@@ -756,22 +773,32 @@ def rotation_timings(case, replays=100, warmup=20):
     torch.cuda.set_device(dev)
     err = torch.zeros((1,), dtype=torch.int32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty((2 * l2,), dtype=torch.uint8, device=dev)
+    restore = None
+    extra = {}
     if case == "c128_decode":
         first = synth.c128_decode(dev, seed=100)
         nbytes = c128_decode_bytes(first)[0]
+        R = max(2, math.ceil(4 * l2 / nbytes))
 
         def make(r):
-            return first if r == 0 else synth.c128_decode(dev, seed=100 + r)
+            d = first if r == 0 else synth.c128_decode(dev, seed=100 + r)
+            d["state0"] = d["state"].clone()
+            return d
 
         def call(d, pdl):
             ck.ckv_c128_online_decode(d["state"], d["input"], d["out"], d["ape"], d["indices"], d["seq_lens"],
                                       use_pdl=pdl, err_word=err)
+
+        def restore(inst):
+            for d in inst:
+                d["state"].copy_(d["state0"])
     elif case == "kpool_decode":
         first = synth.pooled_decode(dev, seed=100)
         nbytes = kpool_decode_bytes(first)[0]
         B, ps = first["B"], first["page_size"]
-        R0 = max(2, math.ceil(4 * l2 / nbytes))
-        cache = torch.zeros(((R0 * B + ps - 1) // ps, ps, first["D"] + 4), device=dev, dtype=torch.uint8)
+        R = max(2, math.ceil(4 * l2 / nbytes))
+        cache = torch.zeros(((R * B + ps - 1) // ps, ps, first["D"] + 4), device=dev, dtype=torch.uint8)
 
         def make(r):
             d = first if r == 0 else synth.pooled_decode(dev, seed=100 + r)
@@ -783,24 +810,54 @@ def rotation_timings(case, replays=100, warmup=20):
 
         def call(d, pdl):
             ck.ckv_kpool_decode_update(d["kv_cache"], d["ring"], d["tail_slot_mapping"], d["slot_mapping"],
-                                       d["positions"], d["key"], d["score"], d["ape"], round_scale=True,
+                                       d["positions"], d["key"], d["score"], d["ape"], round_scale=round_scale,
                                        use_pdl=pdl, err_word=err)
+    elif case.startswith("latency_floor"):
+        # same instance count as the pooled decode's cold timing
+        nbytes = kpool_decode_bytes(synth.pooled_decode("cpu", seed=100))[0]
+        R = max(2, math.ceil(4 * l2 / nbytes))
+        hops = int(case[-1])
+        n = 512
+        g = torch.Generator(device=dev)
+        g.manual_seed(7)
+
+        def make(r):
+            return {"idx": torch.randperm(n, generator=g, device=dev).to(torch.int32),
+                    "rows": torch.randint(0, 255, (n, 256), generator=g, device=dev, dtype=torch.uint8),
+                    "out": torch.zeros((n, 256), device=dev, dtype=torch.uint8)}
+
+        def call(d, pdl):
+            ck.ckv_latency_probe(hops, n, d["idx"], d["rows"], d["out"], warps_per_cta=4, use_pdl=pdl)
+
+        nbytes = n * 4 + (n * 512 if hops == 2 else n * 4 if hops == 1 else 0)
     else:
-        raise SystemExit("--rotate applies to --case c128_decode or kpool_decode")
-    R = max(2, math.ceil(4 * l2 / nbytes))
+        raise SystemExit("--rotate applies to --case c128_decode, kpool_decode or latency_floor0|1|2")
     inst = [make(r) for r in range(R)]
+    flush_each = restore is not None or case.startswith("latency_floor")
     peak, peak_kind = _peaks()
     stream = torch.cuda.Stream(dev)
     res = {"case": case, "mode": "rotate", "instances": R, "l2_bytes": l2, "bytes_per_call": nbytes,
-           "replays": replays}
+           "replays": replays, "l2_flush_before_each_replay": flush_each}
+    if case == "kpool_decode":
+        res["round_scale"] = bool(round_scale)
 
-    def timed(graph, n_calls):
+    def before(warm):
+        # cold: every instance restored, then L2 flushed; warm: the one instance
+        # restored (its state then sits in L2), nothing flushed
+        if restore is not None:
+            restore(inst[:1] if warm else inst)
+        if flush_each and not warm:
+            flush.zero_()
+
+    def timed(graph, n_calls, warm=False):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t = []
         with torch.cuda.stream(stream):
             for _ in range(max(20, warmup)):
+                before(warm)
                 graph.replay()
             for _ in range(replays):
+                before(warm)
                 e0.record(stream)
                 graph.replay()
                 e1.record(stream)
@@ -808,6 +865,24 @@ def rotation_timings(case, replays=100, warmup=20):
                 t.append(e0.elapsed_time(e1) * 1e3 / n_calls)
         return float(np.median(t))
 
+    if case == "c128_decode":
+        # bytes the call physically writes: the max-row sectors (8 channels, 32
+        # bytes) of open requests whose new maxima equal the stored ones are left
+        # alone by the kernel
+        with torch.cuda.stream(stream):
+            restore(inst)
+            d = inst[0]
+            before_max = d["state"][:, 0].clone()
+            call(d, False)
+        stream.synchronize()
+        p = (d["seq_lens"].to(torch.int64) - 1) % 128
+        open_ = (p != 0) & (p != 127)
+        rows = d["indices"].to(torch.int64)[open_]
+        same = (d["state"][rows, 0].view(torch.int32) == before_max[rows].view(torch.int32))
+        kept = int(same.view(same.shape[0], -1, 8).all(dim=2).sum())
+        extra = {"max_sectors_left_alone": kept, "physical_bytes_per_call": nbytes - 32 * kept,
+                 "max_moved_fraction": round(1.0 - float(same.float().mean()), 4) if rows.numel() else 0.0}
+        res.update(extra)
     for pdl in (True, False):
         with torch.cuda.stream(stream):
             for d in inst:
@@ -822,10 +897,14 @@ def rotation_timings(case, replays=100, warmup=20):
             call(inst[0], pdl)
         tag = "pdl" if pdl else "no_pdl"
         us_cold = timed(cold, R)
-        us_warm = timed(warm, 1)
+        us_warm = timed(warm, 1, warm=True)
         res[tag] = {"us_per_call_cold": round(us_cold, 3), "gbs_cold": round(nbytes / us_cold / 1e3, 1),
                     f"frac_of_{peak_kind}_hbm": round(nbytes / us_cold / 1e3 / peak, 4),
                     "us_single_call_warm": round(us_warm, 3)}
+        if "physical_bytes_per_call" in extra:
+            res[tag]["gbs_cold_physical"] = round(extra["physical_bytes_per_call"] / us_cold / 1e3, 1)
+            res[tag][f"frac_of_{peak_kind}_hbm_physical"] = round(
+                extra["physical_bytes_per_call"] / us_cold / 1e3 / peak, 4)
         del cold, warm
     torch.cuda.synchronize()
     res["err"] = int(err.item())
@@ -844,6 +923,8 @@ def main():
     ap.add_argument("--rotate", action="store_true",
                     help="with --case c128_decode|kpool_decode: L2-cold and warm per-call time from CUDA graph "
                          "replays over rotating instances (--steps replays, median)")
+    ap.add_argument("--linear-scale", action="store_true",
+                    help="with --case kpool_decode --rotate: the linear FP8 scale instead of the power-of-two one")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
@@ -928,17 +1009,24 @@ def main():
         elapsed_ms = e_start.elapsed_time(e_end)
         # breakdown: the same steps with an event between consecutive calls (an event
         # between two launches removes the programmatic overlap, so this loop is
-        # timed on its own and used only to attribute time to the five calls)
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(K)]
+        # timed on its own and used only to attribute time to the five calls).
+        # Every other step of this loop runs the pooled decode with the linear FP8
+        # scale instead of the power-of-two one, in the same place of the step.
+        Kb = 2 * K
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(Kb)]
         torch.cuda.synchronize()
-        for k in range(K):
+        for k in range(Kb):
             evs[k][0].record(stream)
             for i in range(nk):
+                step.round_scale = (k % 2 == 0) or i != 0
                 step.call(i, False)
                 evs[k][i + 1].record(stream)
+        step.round_scale = True
         stream.synchronize()
-        breakdown_ms = evs[0][0].elapsed_time(evs[-1][nk]) / K
-    per_kernel_ms = [statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)) for i in range(nk)]
+        breakdown_ms = statistics.mean(evs[k][0].elapsed_time(evs[k][nk]) for k in range(0, Kb, 2))
+    per_kernel_ms = [statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(0, Kb, 2))
+                     for i in range(nk)]
+    linear_ms = statistics.mean(evs[k][0].elapsed_time(evs[k][1]) for k in range(1, Kb, 2))
     elapsed_ms = _max_over_ranks(elapsed_ms, ws, dev)
     ms_per_step = elapsed_ms / K
     tokens_step = sum(step.tokens)
@@ -951,6 +1039,14 @@ def main():
                       "frac_of_" + peak_kind + "_peak": round(gbs / peak, 4), "tokens": int(step.tokens[i]),
                       "compressed_rows": int(step.rows[i]),
                       "tokens_per_s": round(step.tokens[i] / (per_kernel_ms[i] / 1e3), 1)}
+    kernels["kpool_decode_update_linear_scale"] = {
+        "us": round(linear_ms * 1e3, 2), "bytes": int(step.bytes[0]),
+        "frac_of_" + peak_kind + "_peak": round(step.bytes[0] / (linear_ms / 1e3) / 1e9 / peak, 4),
+        "note": "the pooled decode call with the linear FP8 scale, timed in the same place of the step (not part "
+                "of the step's tokens)"}
+    kernels["c128_online_decode"]["note"] = (
+        "every step replays the same tokens into the same slots, so after the first step no running max moves; "
+        "decode_l2_cold times it on restored states")
     dom = max(range(nk), key=lambda i: per_kernel_ms[i])
     dom_gbs = step.bytes[dom] / (per_kernel_ms[dom] / 1e3) / 1e9
     tr = NCU_TRAFFIC.get(step.names[dom])
@@ -1009,14 +1105,28 @@ def main():
     decode_cold = None
     if rank == 0 and ws == 1 and not args.no_decode_cold:  # rotating instances on the one GPU
         decode_cold = {}
-        for name, case in (("kpool_decode_update", "kpool_decode"), ("c128_online_decode", "c128_decode")):
-            r = rotation_timings(case)
-            decode_cold[name] = {"instances": r["instances"], "bytes_per_call": r["bytes_per_call"],
-                                 "us_per_call_cold": r["pdl"]["us_per_call_cold"], "gbs_cold": r["pdl"]["gbs_cold"],
-                                 "frac": r["pdl"][f"frac_of_{peak_kind}_hbm"],
-                                 "us_single_call_warm": r["pdl"]["us_single_call_warm"], "err": r["err"]}
+        for name, case, rs in (("kpool_decode_update", "kpool_decode", True),
+                               ("kpool_decode_update_linear_scale", "kpool_decode", False),
+                               ("c128_online_decode", "c128_decode", True),
+                               ("latency_floor_2hops", "latency_floor2", True),
+                               ("latency_floor_0hops", "latency_floor0", True)):
+            r = rotation_timings(case, round_scale=rs)
+            e = {"instances": r["instances"], "bytes_per_call": r["bytes_per_call"],
+                 "us_per_call_cold": r["pdl"]["us_per_call_cold"], "gbs_cold": r["pdl"]["gbs_cold"],
+                 "frac": r["pdl"][f"frac_of_{peak_kind}_hbm"],
+                 "us_single_call_warm": r["pdl"]["us_single_call_warm"], "err": r["err"]}
+            for k in ("physical_bytes_per_call", "max_moved_fraction"):
+                if k in r:
+                    e[k] = r[k]
+            if "gbs_cold_physical" in r["pdl"]:
+                e["frac_physical"] = r["pdl"][f"frac_of_{peak_kind}_hbm_physical"]
+            decode_cold[name] = e
         decode_cold["method"] = ("R instances (R x bytes per call >= 4 x L2), one call on each, captured in order "
-                                 "in one CUDA graph with programmatic dependent launch; median of 100 replays / R")
+                                 "in one CUDA graph with programmatic dependent launch; median of 100 replays / R. "
+                                 "c128 decode: every state pool restored from a pristine copy and a 2 x L2 buffer "
+                                 "written before each replay (outside the events). latency_floor: the probe "
+                                 "kernels in the pooled decode's launch shape (512 warps, 4 per CTA), L2 flushed "
+                                 "before each replay")
 
     if rank == 0:
         print(json.dumps({

@@ -20,6 +20,7 @@ from .ckv import (  # noqa: F401
     ckv_kpool_compress_set_variant,
     ckv_kpool_decode_update,
     ckv_kpool_seed_tail,
+    ckv_latency_probe,
     ckv_plan_online_prefill,
     ckv_plan_online_prefill_device,
     ckv_wait_timeout_selftest,

@@ -20,7 +20,7 @@ LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libckv.so")
 
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
-CUDA_SOURCES = ["kpool.cu", "c128.cu", "prefill_tma.cu", "planner_device.cu", "validate.cu", "capi.cu"]
+CUDA_SOURCES = ["kpool.cu", "c128.cu", "prefill_tma.cu", "planner_device.cu", "validate.cu", "probe.cu", "capi.cu"]
 CXX_SOURCES = ["planner.cpp"]
 
 

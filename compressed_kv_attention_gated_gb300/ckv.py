@@ -40,6 +40,7 @@ _STATUS_FUNCS = {
     "ckv_wait_timeout_selftest": 3,
     "ckv_check_distinct": 8,
     "ckv_check_distinct_noalloc": 6,
+    "ckv_latency_probe": 9,
 }
 EXPORTED = tuple(_STATUS_FUNCS) + ("ckv_status_string", "ckv_last_cuda_error", "ckv_abi_version",
                                     "ckv_c128_prefill_set_variant", "ckv_kpool_compress_set_variant")
@@ -135,6 +136,9 @@ def load():
                 ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
             L.ckv_check_distinct_noalloc.argtypes = [
                 ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+            L.ckv_latency_probe.argtypes = [
+                ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32,
+                ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
             L.ckv_status_string.restype = ctypes.c_char_p
             L.ckv_status_string.argtypes = [ctypes.c_int32]
             L.ckv_last_cuda_error.restype = ctypes.c_int32
@@ -592,3 +596,25 @@ def ckv_check_distinct_noalloc(ids, id_range, err_word, stream=None):
     _need(err_word.dtype == torch.int32, "err_word must be int32")
     _check("ckv_check_distinct_noalloc", L.ckv_check_distinct_noalloc(
         _ptr(ids), ids.element_size(), ids.numel(), int(id_range), _ptr(err_word), _stream(stream, ids)))
+
+
+def ckv_latency_probe(hops, n_warps, idx=None, rows=None, out=None, warps_per_cta=4, use_pdl=False, stream=None):
+    """Latency floor of a decode-sized launch (see include/ckv.h): hops 0, 1 or
+    2 dependent global round trips per warp.  idx int32 [n_warps]; rows and out
+    uint8 [*, 256]; stream defaults to the current stream."""
+    L = load()
+    _cuda("ckv_latency_probe", idx, rows, out)
+    if idx is not None:
+        _need(idx.dtype == torch.int32 and idx.is_contiguous() and idx.numel() >= n_warps, "idx must be int32 [n_warps]")
+    for t in (rows, out):
+        if t is not None:
+            _need(t.dtype == torch.uint8 and t.is_contiguous() and t.dim() == 2 and t.shape[1] == 256,
+                  "rows/out must be contiguous uint8 [n, 256]")
+    if out is not None:
+        _need(out.shape[0] >= n_warps, "out must have n_warps rows")
+    num_rows = rows.shape[0] if rows is not None else 0
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    strm = ctypes.c_void_p(stream if isinstance(stream, int) else stream.cuda_stream)
+    _check("ckv_latency_probe", L.ckv_latency_probe(int(hops), _ptr(idx), _ptr(rows), num_rows, _ptr(out),
+                                                    int(n_warps), int(warps_per_cta), int(bool(use_pdl)), strm))

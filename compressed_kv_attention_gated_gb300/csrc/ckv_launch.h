@@ -170,4 +170,9 @@ int64_t noalloc_check_max_range();
 cudaError_t launch_check_distinct_noalloc(const void* ids, int id_bytes, int64_t n, int64_t range, int32_t* err,
                                           cudaStream_t s);
 
+// probe.cu: latency floors of a decode-sized launch (hops 0, 1 or 2 dependent
+// global round trips per warp).
+cudaError_t launch_latency_probe(int hops, const int32_t* idx, const void* rows, int64_t num_rows, void* out,
+                                 int32_t n_warps, int32_t warps_per_cta, bool use_pdl, cudaStream_t s);
+
 }  // namespace ckv

@@ -1,0 +1,59 @@
+// probe.cu -- latency floors of a decode-sized launch (a measurement aid).
+//
+// The pooled decode update is bound by latency, not bandwidth: one call moves
+// about 3 MB, and a closing pool needs two dependent global round trips (its
+// token's index words, then the ring rows they name).  These kernels have the
+// decode kernel's launch shape (one warp per request, a few warps per CTA) and
+// do nothing but the dependent memory traffic of that critical path, so that
+// timing them with the same method as the decode call gives its floor:
+//   hops 0  wait for the predecessor grid (programmatic dependent launch) and
+//           return: the launch-and-completion cost alone;
+//   hops 1  each warp loads the 4-byte word idx[w] and lane 0 stores it: one
+//           global round trip;
+//   hops 2  each warp loads idx[w], then the 256-byte row rows[idx[w]] (8 bytes
+//           per lane), then stores that row: two dependent round trips.
+// An index outside [0, num_rows) is skipped.
+#include <cstdint>
+
+#include "ckv_device.cuh"
+#include "ckv_launch_util.cuh"
+
+namespace ckv {
+namespace {
+
+template <int kHops>
+__global__ void latency_probe_kernel(const int32_t* idx, const uint2* rows, int64_t num_rows, uint2* out,
+                                     int32_t n_warps) {
+  pdl_wait();
+  pdl_trigger();
+  if constexpr (kHops > 0) {
+    const int lane = threadIdx.x & 31;
+    const int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (w >= n_warps) return;
+    const int32_t r = idx[w];
+    if constexpr (kHops == 1) {
+      if (lane == 0) reinterpret_cast<int32_t*>(out + w * 32)[0] = r;
+    } else {
+      if (r < 0 || r >= num_rows) return;
+      out[w * 32 + lane] = rows[static_cast<int64_t>(r) * 32 + lane];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_latency_probe(int hops, const int32_t* idx, const void* rows, int64_t num_rows, void* out,
+                                 int32_t n_warps, int32_t warps_per_cta, bool use_pdl, cudaStream_t s) {
+  const unsigned ctas = static_cast<unsigned>((n_warps + warps_per_cta - 1) / warps_per_cta);
+  const dim3 grid(ctas > 0 ? ctas : 1u), block(32 * warps_per_cta);
+  const uint2* r = static_cast<const uint2*>(rows);
+  uint2* o = static_cast<uint2*>(out);
+  switch (hops) {
+    case 0: return launch_ex(latency_probe_kernel<0>, grid, block, 0, use_pdl, s, idx, r, num_rows, o, n_warps);
+    case 1: return launch_ex(latency_probe_kernel<1>, grid, block, 0, use_pdl, s, idx, r, num_rows, o, n_warps);
+    case 2: return launch_ex(latency_probe_kernel<2>, grid, block, 0, use_pdl, s, idx, r, num_rows, o, n_warps);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace ckv

@@ -67,6 +67,19 @@ def random_states(num_slots, D, g, device):
     return st
 
 
+def prior_chunk_tokens(seq_lens, D, seed, device="cpu", dtype=F32):
+    """Virtual earlier tokens of each request's current 128-token chunk: the
+    new token of request b sits at chunk position p_b = (seq_lens[b] - 1) % 128,
+    so p_b tokens (kv | score ~ N(0, 1)) came before it in its chunk.  They are
+    laid out request after request in one ragged array [sum p_b, 2D]; a
+    caller builds a consistent running state from them.  Returns (rows, p)."""
+    seq = torch.as_tensor(seq_lens, dtype=torch.int64).cpu()
+    p = (seq - 1) % 128
+    g = _gen(device, seed)
+    rows = _randn((int(p.sum()), 2 * D), g, device, dtype=dtype)
+    return rows, p
+
+
 # ---------------------------------------------------------------- pooled P=16
 def tiny_pooled(device="cpu", seed=0, B=4, N=64, P=16, D=128, page_size=64):
     """B requests with positions 0..N-1 each; request b uses tail block b and

@@ -443,6 +443,28 @@ ckv_status ckv_c128_online_prefill_counted_fp8(float* state, int64_t num_slots, 
                                                const int64_t* cache_loc, int32_t round_scale,
                                                int32_t use_pdl, int32_t* err_word, void* stream);
 
+/*
+ * Latency floor of a decode-sized launch: a measurement aid with no
+ * counterpart in the sources.  Launches n_warps warps, warps_per_cta to a CTA
+ * (the pooled decode update's launch shape is one warp per request, 4 to a
+ * CTA), each of which first waits for the preceding grid when use_pdl is set
+ * (programmatic dependent launch), then does only dependent memory traffic:
+ *   hops == 0  nothing (the cost of launching and completing the grid);
+ *   hops == 1  loads idx[w] and stores it to the first 4 bytes of row w of out
+ *              (one global round trip);
+ *   hops == 2  loads idx[w], then row idx[w] of rows, and stores it as row w
+ *              of out (two dependent round trips, as when a closing pool's
+ *              index words name the ring rows it reads).
+ *   idx        device int32 [n_warps] (hops >= 1); an index outside
+ *              [0, num_rows) makes that warp skip its row
+ *   rows       device [num_rows][256 bytes], 8-byte aligned (hops == 2)
+ *   out        device [n_warps][256 bytes], 8-byte aligned (hops >= 1)
+ * Sizes outside hops 0..2, n_warps >= 1, 1 <= warps_per_cta <= 32 return
+ * CKV_ERR_SHAPE and launch nothing.
+ */
+ckv_status ckv_latency_probe(int32_t hops, const int32_t* idx, const void* rows, int64_t num_rows, void* out,
+                             int32_t n_warps, int32_t warps_per_cta, int32_t use_pdl, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -84,6 +84,51 @@ def test_c128_decode_full_size(ck, ora):
     assert _check_decode(ora, d, g_state, g_out) >= 3
 
 
+def test_c128_decode_full_size_states_from_prior_tokens(ck, ora):
+    """Full size (2048 requests, D=512, 4096 slots) with every touched slot
+    holding the state of its chunk's earlier tokens: p = (seq_len - 1) % 128
+    virtual tokens drawn like the input, reduced by the oracle's two-pass.  The
+    closing rows must then equal a two-pass over all 128 tokens of the chunk,
+    and the new states the two-pass over its p + 1 tokens (sglang page
+    c128_online.cuh, flash_c128_online_decode; consistent initial states)."""
+    from compressed_kv_attention_gated_gb300 import synth
+
+    d = synth.c128_decode("cpu", seed=11)
+    D, B = d["D"], d["B"]
+    d["seq_lens"][:4] = torch.tensor([128, 1, 2, 131072], dtype=torch.int32)
+    seq = d["seq_lens"].numpy().astype(np.int64)
+    prior, p = synth.prior_chunk_tokens(seq, D, seed=12)
+    p = p.numpy()
+    ape = f32(d["ape"])
+    idx = d["indices"].numpy()
+    chunk0 = seq - 1 - p  # position of the chunk's first token
+    has = p > 0
+    zeros = np.zeros((1, 3, D), np.float32)
+    _, _, fs, sw = ora.c128_prefill(zeros, f32(prior), ape, np.zeros(int(has.sum()), np.int32),
+                                    chunk0[has] + p[has], p[has])
+    assert sw.all()
+    state = d["state"].clone()
+    state[torch.from_numpy(idx[has]).long()] = torch.from_numpy(fs.astype(np.float32))
+    d["state"] = state
+    g_state, g_out, err = _decode_gpu(ck, d)
+    assert err == 0
+    n_closed = _check_decode(ora, d, g_state, g_out)
+    assert n_closed >= 5
+    # the whole chunk so far (prior tokens, then the new one) as one prefill segment per request
+    starts = np.concatenate([[0], np.cumsum(p)])
+    full = np.concatenate([np.concatenate([f32(prior)[starts[b]:starts[b + 1]], f32(d["input"])[b:b + 1]])
+                           for b in range(B)])
+    out2, written, fs2, sw2 = ora.c128_prefill(zeros, full, ape, np.zeros(B, np.int32), seq, p + 1)
+    last = np.cumsum(p + 1) - 1
+    closed = p == 127
+    assert np.all(written[last] == closed) and np.all(sw2 == ~closed)
+    assert_close_rel(g_out[closed], out2[last[closed]], "closing rows vs two-pass over the chunk")
+    gs = g_state[idx[~closed]]
+    assert_close_abs(gs[:, 0], fs2[~closed, 0], what="max vs two-pass")
+    assert_close_rel(gs[:, 1], fs2[~closed, 1], "sum vs two-pass")
+    assert_close_rel(gs[:, 2], fs2[~closed, 2], "kv vs two-pass")
+
+
 @pytest.mark.parametrize("D", [128, 256, 512])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("use_pdl", [False, True])

@@ -7,12 +7,15 @@ For every call: the state and fp32 rows equal the plain call's bit for bit;
 every byte of the cache equals the oracle's store of the GPU's own fp32 rows
 (bf16, Hadamard-128, bf16 and absmax FP8 are deterministic given the fp32
 row, so this is exact), bytes of other rows keep their canary; leaving out
-the fp32 rows gives the same cache; a bad location is flagged and skipped."""
+the fp32 rows gives the same cache; a bad location is flagged and skipped.
+End to end, against the oracle's store of its OWN rows: every 128-channel
+block whose bf16 rounding agrees has identical codes and scale, and the
+blocks that differ are bounded by the bf16 flips the fp32 error explains."""
 import numpy as np
 import pytest
 import torch
 
-from helpers import assert_close_rel, bf16_bits, f32, u8
+from helpers import assert_close_rel, bf16_bits, bf16_flip_check, f32, report, u8
 
 pytestmark = pytest.mark.gpu
 CANARY = 0x5A
@@ -48,6 +51,41 @@ def _expect(ora, cache0, ps, rows, locs, round_scale):
 
 def _input_np(t):
     return bf16_bits(t) if t.dtype == torch.bfloat16 else f32(t)
+
+
+def _bf16_of(x):
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(
+        np.uint16)
+
+
+def _block_bytes(cache, ps, D, loc, j):
+    """(codes, scale bits) of 128-channel block j of the row at loc."""
+    nb = D // 128
+    flat = cache.reshape(-1)
+    page, tok = divmod(int(loc), ps)
+    base = page * ps * (D + 4 * nb)
+    codes = flat[base + tok * D + 128 * j: base + tok * D + 128 * j + 128]
+    sc = flat[base + ps * D + 4 * (tok * nb + j): base + ps * D + 4 * (tok * nb + j) + 4]
+    return codes, sc
+
+
+def check_vs_oracle_rows(ora, gpu_cache, cache0, ps, gpu_rows, ref_rows, locs, round_scale, what):
+    """The GPU's FP8 cache against the oracle's store of the oracle's own rows:
+    identical bytes on every block whose bf16 rounding agrees; flips bounded."""
+    D = gpu_rows.shape[1]
+    nb = D // 128
+    r32 = np.asarray(ref_rows, np.float32)
+    ref = _expect(ora, cache0, ps, r32, locs, round_scale)
+    xg, xr = _bf16_of(gpu_rows), _bf16_of(r32)
+    bf16_flip_check(gpu_rows, xg, r32, xr, what)
+    same = np.all((xg == xr).reshape(len(locs), nb, 128), axis=2)
+    for i, loc in enumerate(locs):
+        for j in range(nb):
+            gc, gsc = _block_bytes(gpu_cache, ps, D, loc, j)
+            rc, rsc = _block_bytes(ref, ps, D, loc, j)
+            if same[i, j]:
+                assert np.array_equal(gc, rc) and np.array_equal(gsc, rsc), (what, i, j)
+    report(what + " blocks", blocks=int(same.size), blocks_differing_bf16=int((~same).sum()))
 
 
 @pytest.mark.parametrize("round_scale", [True, False])
@@ -91,6 +129,8 @@ def test_decode_fp8(ck, ora, D, dtype, round_scale):
     ref = _expect(ora, cache0, ps, f32(out_f)[closed], cache_loc.numpy()[closed], round_scale)
     np.testing.assert_array_equal(u8(cache), ref)
     np.testing.assert_array_equal(u8(cache_n), ref)
+    check_vs_oracle_rows(ora, u8(cache), cache0, ps, f32(out_f)[closed], out_ref[closed], cache_loc.numpy()[closed],
+                         round_scale, f"c128 decode fp8 D={D} {dtype} round={round_scale}")
 
 
 def _prefill(ck, d, cp, wp, nc, nw, out, cache, cache_loc, round_scale, use_pdl, err, fp8=True):
@@ -135,6 +175,12 @@ def test_prefill_fp8(variant, ck, ora, D, dtype, round_scale, use_pdl):
     ref = _expect(ora, cache0, ps, f32(out_f)[rows], cache_loc.numpy()[rows], round_scale)
     np.testing.assert_array_equal(u8(cache), ref)
     np.testing.assert_array_equal(u8(cache_n), ref)
+    out_ref, written, _, _ = ora.c128_prefill(f32(d["state"]), _input_np(d["input"]), f32(d["ape"]),
+                                              d["indices"].numpy(), d["seq_lens"].numpy(), d["extend_lens"].numpy())
+    assert np.array_equal(np.nonzero(written)[0], np.sort(rows))
+    check_vs_oracle_rows(ora, u8(cache), cache0, ps, f32(out_f)[rows], out_ref[rows], cache_loc.numpy()[rows],
+                         round_scale, f"c128 prefill fp8 D={D} {dtype} round={round_scale} pdl={use_pdl} "
+                                      f"variant={variant}")
 
 
 def test_prefill_fp8_long_context_full(ck, ora):
@@ -158,6 +204,12 @@ def test_prefill_fp8_long_context_full(ck, ora):
     g = f32(out.index_select(0, torch.from_numpy(rows).cuda()))
     ref = _expect(ora, cache0, ps, g, cache_loc.numpy()[rows], True)
     np.testing.assert_array_equal(u8(cache), ref)
+    out_ref, written, _, _ = ora.c128_prefill(f32(d["state"]), bf16_bits(d["input"]), f32(d["ape"]),
+                                              d["indices"].cpu().numpy(), d["seq_lens"].numpy(),
+                                              d["extend_lens"].numpy())
+    assert np.array_equal(np.nonzero(written)[0], rows)
+    check_vs_oracle_rows(ora, u8(cache), cache0, ps, g, out_ref[rows], cache_loc.numpy()[rows], True,
+                         "c128 prefill fp8 long context 8x131072")
 
 
 def test_fp8_bad_location_flagged_and_skipped(ck, ora):

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import assert_close_rel, bf16_bits, cache_rows, f32, u8
+from helpers import assert_close_rel, bf16_bits, bf16_flip_check, bf16_values, cache_rows, f32, u8
 
 pytestmark = pytest.mark.gpu
 
@@ -52,7 +52,18 @@ def ora_bf16_bits(x):
 
 
 def check_rows(ora, gpu_x, gpu_xb, gpu_yb, gpu_q, gpu_s, ref, round_scale, what):
-    """Stage-wise and end-to-end comparison of pooled rows."""
+    """Stage-wise and end-to-end comparison of pooled rows.
+
+    The chain x -> bf16 -> rotation -> bf16 -> FP8 is checked link by link:
+    x within the tolerance; the GPU's bf16 row is the round-to-nearest-even of
+    its own x; it differs from the oracle's bf16 row only in channels where a
+    rounding boundary lies between the two x values, no more often than the
+    measured fp32 error makes likely (bf16_flip_check); the oracle's rotation
+    of the GPU's bf16 row is the GPU's rotated row and the oracle's quantiser
+    of that gives the GPU's codes and scale, bit for bit.  So rows whose bf16
+    row agrees have the oracle's codes and scale exactly, and every other row
+    is the exact image of a legitimately rounded bf16 row.  Returns the
+    number of rows with a flipped bf16 channel."""
     assert_close_rel(gpu_x, ref["x"], what + " x")
     np.testing.assert_array_equal(ora.rotate_bf16(gpu_xb), gpu_yb, err_msg=what + " rotation stage")
     q2, s2 = ora.quantize_rows(gpu_yb, round_scale)
@@ -61,18 +72,40 @@ def check_rows(ora, gpu_x, gpu_xb, gpu_yb, gpu_q, gpu_s, ref, round_scale, what)
     same = np.all(gpu_xb == ref["xb"], axis=1)
     np.testing.assert_array_equal(gpu_q[same], ref["q"][same], err_msg=what + " codes (same xb rows)")
     np.testing.assert_array_equal(gpu_s[same].view(np.uint32), ref["scale"][same].view(np.uint32))
-    # first rounding stage: the GPU's bf16 row is the round-to-nearest-even of its
-    # own fp32 pooled row (rows whose x sits near a bf16 rounding boundary may
-    # round differently from the oracle's exact x; x itself is within tolerance)
-    diff = ~same
     np.testing.assert_array_equal(ora_bf16_bits(gpu_x), gpu_xb, err_msg=what + " bf16 rounding stage")
-    # every row, whichever side of a bf16 boundary its x fell: the dequantised rows
-    # agree within one FP8 step at the top of the row's range
-    dq_g = e4m3_values(gpu_q) * gpu_s[:, None].astype(np.float64)
-    dq_r = e4m3_values(ref["q"]) * ref["scale"][:, None].astype(np.float64)
-    top = np.max(np.abs(dq_r), axis=1, keepdims=True)
-    assert np.all(np.abs(dq_g - dq_r) <= 0.08 * top + 1e-30), what + " dequantised rows"
-    return int(diff.sum())
+    rows, _, _ = bf16_flip_check(gpu_x, gpu_xb, ref["x"], ref["xb"], what)
+    check_dequantised(gpu_xb, gpu_yb, gpu_q, gpu_s, ref, what)
+    return rows
+
+
+def _bf16_half_ulp(v):
+    a = np.maximum(np.abs(v), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(a)) - 8)
+
+
+def _e4m3_half_quantum(t):
+    """Half the spacing of e4m3 values around |t| (3 mantissa bits; subnormal spacing 2^-9)."""
+    a = np.maximum(np.abs(t), 2.0 ** -6)
+    return np.exp2(np.floor(np.log2(a)) - 4)
+
+
+def check_dequantised(gpu_xb, gpu_yb, gpu_q, gpu_s, ref, what):
+    """End to end in value space, with bounds derived per element: the rotated
+    rows differ by no more than the rotation of the bf16 difference (its 1-norm
+    over sqrt(128)) plus the two bf16 roundings and the fp32 butterfly's
+    rounding; the dequantised codes differ by no more than that plus half an
+    e4m3 step of each side at its own scale."""
+    xg, xr = bf16_values(gpu_xb), bf16_values(ref["xb"])
+    yg, yr = bf16_values(gpu_yb), bf16_values(ref["yb"])
+    dx = np.abs(xg - xr).sum(axis=1, keepdims=True) / np.sqrt(128.0)
+    top = np.maximum(np.abs(yg).max(axis=1, keepdims=True), np.abs(yr).max(axis=1, keepdims=True))
+    bound_y = dx * (1 + 1e-6) + _bf16_half_ulp(yg) + _bf16_half_ulp(yr) + 2.0 ** -20 * top
+    assert np.all(np.abs(yg - yr) <= bound_y), what + " rotated rows"
+    sg = gpu_s.astype(np.float64)[:, None]
+    sr = ref["scale"].astype(np.float64)[:, None]
+    dq_g, dq_r = e4m3_values(gpu_q) * sg, e4m3_values(ref["q"]) * sr
+    bound_q = np.abs(yg - yr) + sg * _e4m3_half_quantum(yg / sg) + sr * _e4m3_half_quantum(yr / sr)
+    assert np.all(np.abs(dq_g - dq_r) <= bound_q * (1 + 1e-6)), what + " dequantised rows"
 
 
 # ------------------------------------------------------------------ one-shot
@@ -107,7 +140,8 @@ def test_kpool_compress_vs_oracle(cvariant, ck, ora, P, round_scale):
     ref = ora.kpool_compress(ref_cache, ps, bf16_bits(slot_k), bf16_bits(slot_s), f32(ape), loc.numpy(),
                              return_compressed=True, round_scale=round_scale, taps=True)
     gq, gs = u8(out_q), f32(out_s)
-    check_rows(ora, f32(tx), bf16_bits(txb), bf16_bits(tyb), gq, gs, ref, round_scale, f"P={P}")
+    check_rows(ora, f32(tx), bf16_bits(txb), bf16_bits(tyb), gq, gs, ref, round_scale,
+               f"one-shot P={P} round={round_scale} variant={cvariant}")
     # the cache holds the same rows at loc, and nothing else changed
     gcache = u8(cache)
     cq, cs = cache_rows(gcache, ps, D, loc.numpy())
@@ -136,23 +170,24 @@ def test_kpool_compress_write_mask_and_cache_only(cvariant, ck, ora):
     loc = torch.arange(n, dtype=torch.int64)
     cache0 = torch.full((pages, ps, D + 4), 0xC3, dtype=torch.uint8)
     cache = cache0.cuda()
+    tx = torch.full((n, D), float("nan"), device="cuda")
+    txb = torch.zeros((n, D), dtype=torch.bfloat16, device="cuda")
+    tyb = torch.zeros((n, D), dtype=torch.bfloat16, device="cuda")
     ck.ckv_kpool_compress(slot_k.cuda(), slot_s.cuda(), ape.cuda(), kv_cache=cache, loc=loc.cuda(),
-                          write_mask=wm.cuda())
+                          write_mask=wm.cuda(), tap_x=tx, tap_xb=txb, tap_yb=tyb)
     torch.cuda.synchronize()
     ref_cache = u8(cache0).copy()
-    ora.kpool_compress(ref_cache, ps, bf16_bits(slot_k), bf16_bits(slot_s), f32(ape), loc.numpy(),
-                       write_mask=wm.numpy().astype(np.uint8))
+    ref = ora.kpool_compress(ref_cache, ps, bf16_bits(slot_k), bf16_bits(slot_s), f32(ape), loc.numpy(),
+                             write_mask=wm.numpy().astype(np.uint8), taps=True)
     g_cache = u8(cache)
     gq, gs = cache_rows(g_cache, ps, D, loc.numpy())
     rq, rs = cache_rows(ref_cache, ps, D, loc.numpy())
     w = wm.numpy()
     assert np.all(gq[~w] == 0xC3)
-    # written rows: exact wherever the pooled bf16 rows agree (checked with taps in the
-    # tests above); here, the dequantised rows agree within one FP8 step of their range
-    dq_g = e4m3_values(gq[w]) * gs[w][:, None].astype(np.float64)
-    dq_r = e4m3_values(rq[w]) * rs[w][:, None].astype(np.float64)
-    assert np.all(np.abs(dq_g - dq_r) <= 0.08 * np.max(np.abs(dq_r), axis=1, keepdims=True))
-    assert (gs[w] == rs[w]).mean() > 0.95
+    assert np.all(np.isnan(f32(tx)[~w])), "masked pools computed nothing"
+    sub = {"x": ref["x"][w], "xb": ref["xb"][w], "yb": ref["yb"][w], "q": rq[w], "scale": rs[w]}
+    check_rows(ora, f32(tx)[w], bf16_bits(txb)[w], bf16_bits(tyb)[w], gq[w], gs[w], sub, True,
+               f"write mask variant={cvariant}")
 
 
 def test_kpool_compress_bad_loc_flags_and_skips(cvariant, ck):
@@ -209,7 +244,8 @@ def test_kpool_compress_many_pools_per_warp(cvariant, ck, ora, n, masked):
     rq, rs = cache_rows(ref_cache, ps, D, loc.numpy())
     assert np.all(gq[~w] == 0x11)
     sub = {"x": ref["x"][w], "xb": ref["xb"][w], "yb": ref["yb"][w], "q": rq[w], "scale": rs[w]}
-    check_rows(ora, f32(tx)[w], bf16_bits(txb)[w], bf16_bits(tyb)[w], gq[w], gs[w], sub, True, "many pools")
+    check_rows(ora, f32(tx)[w], bf16_bits(txb)[w], bf16_bits(tyb)[w], gq[w], gs[w], sub, True,
+               f"many pools n={n} masked={masked} variant={cvariant}")
     if not masked:
         np.testing.assert_array_equal(u8(kw["out_fp8"]), gq)
 
@@ -278,7 +314,7 @@ def test_kpool_decode_tiny_in_order_matches_oracle_and_one_shot(ck, ora, round_s
     d = synth.tiny_pooled("cpu", seed=0)
     gpu = _run_decode(ck, d, round_scale)
     oref = _oracle_decode(ora, d, round_scale)
-    n, _ = _compare_decode(ora, d, gpu, oref, round_scale, "tiny decode")
+    n, _ = _compare_decode(ora, d, gpu, oref, round_scale, f"tiny decode round={round_scale}")
     assert n == 16
     # the same 16 pools through the one-shot kernel give bit-identical cache rows
     cache2 = d["kv_cache"].cuda()
@@ -296,9 +332,8 @@ def test_kpool_decode_verify_batch_full_size(ck, ora, round_scale):
     d = synth.pooled_decode("cpu", seed=0 if round_scale else 1)
     gpu = _run_decode(ck, d, round_scale)
     oref = _oracle_decode(ora, d, round_scale)
-    n, ndiff = _compare_decode(ora, d, gpu, oref, round_scale, "decode/verify")
+    n, ndiff = _compare_decode(ora, d, gpu, oref, round_scale, f"decode/verify 512x4 round={round_scale}")
     assert n > 50
-    assert ndiff <= max(2, n // 20)
 
 
 @pytest.mark.parametrize("P", [1, 4, 16])
@@ -318,23 +353,59 @@ def test_kpool_decode_long_sequences_and_across_calls(ck, ora, P):
     rcache = u8(d["kv_cache"]).copy()
     rring = bf16_bits(d["ring"]).copy()
     cuts = [0, 1, P + 2, total]
+    taps_g, taps_r, closing_locs = [], [], []
     for a, b in zip(cuts[:-1], cuts[1:]):
         sl = {k: d[k][:, a:b].contiguous() for k in ("tail_slot_mapping", "slot_mapping", "positions", "key", "score")}
+        n_tok = B * (b - a)
+        tx = torch.full((n_tok, D), float("nan"), device="cuda")
+        txb = torch.zeros((n_tok, D), dtype=torch.bfloat16, device="cuda")
+        tyb = torch.zeros((n_tok, D), dtype=torch.bfloat16, device="cuda")
         ck.ckv_kpool_decode_update(cache_g, ring_g, sl["tail_slot_mapping"].cuda(), sl["slot_mapping"].cuda(),
-                                   sl["positions"].cuda(), sl["key"].cuda(), sl["score"].cuda(), d["ape"].cuda())
-        ora.kpool_decode_update(rcache, d["page_size"], rring, sl["tail_slot_mapping"].numpy(),
-                                sl["slot_mapping"].numpy(), sl["positions"].numpy(), bf16_bits(sl["key"]),
-                                bf16_bits(sl["score"]), f32(d["ape"]))
+                                   sl["positions"].cuda(), sl["key"].cuda(), sl["score"].cuda(), d["ape"].cuda(),
+                                   tap_x=tx, tap_xb=txb, tap_yb=tyb)
+        r = ora.kpool_decode_update(rcache, d["page_size"], rring, sl["tail_slot_mapping"].numpy(),
+                                    sl["slot_mapping"].numpy(), sl["positions"].numpy(), bf16_bits(sl["key"]),
+                                    bf16_bits(sl["score"]), f32(d["ape"]), taps=True)
+        sm = sl["slot_mapping"].numpy().reshape(-1)
+        pos = sl["positions"].numpy().reshape(-1)
+        closing = np.nonzero((sm >= 0) & (pos >= 0) & (pos % P == P - 1))[0]
+        taps_g.append((tx, txb, tyb, closing))
+        taps_r.append({k: v[closing] for k, v in r.items()})
+        closing_locs.append(sm[closing])
     torch.cuda.synchronize()
     np.testing.assert_array_equal(bf16_bits(ring_g), rring)
-    sm = d["slot_mapping"].numpy().reshape(-1)
-    locs = sm[sm >= 0]
+    locs = np.concatenate(closing_locs)
+    assert len(locs) == (total // P) * B
     gq, gs = cache_rows(u8(cache_g), d["page_size"], D, locs)
     rq, rs = cache_rows(rcache, d["page_size"], D, locs)
-    dq_g = e4m3_values(gq) * gs[:, None].astype(np.float64)
-    dq_r = e4m3_values(rq) * rs[:, None].astype(np.float64)
-    assert np.all(np.abs(dq_g - dq_r) <= 0.08 * np.max(np.abs(dq_r), axis=1, keepdims=True))
-    assert (gs == rs).mean() > 0.9
+    gx = np.concatenate([f32(t[0])[t[3]] for t in taps_g])
+    gxb = np.concatenate([bf16_bits(t[1])[t[3]] for t in taps_g])
+    gyb = np.concatenate([bf16_bits(t[2])[t[3]] for t in taps_g])
+    ref = {k: np.concatenate([t[k] for t in taps_r]) for k in ("x", "xb", "yb")}
+    ref["q"], ref["scale"] = rq, rs
+    check_rows(ora, gx, gxb, gyb, gq, gs, ref, True, f"across calls P={P}")
+
+
+def test_kpool_decode_golden_gating_and_block_clamp(ck):
+    """The hand-derived pooled-decode fixture (closing token with a negative
+    tail slot reads ring block 0 and stashes nothing; closing slot without a
+    cache location only stashes; open slot with a negative tail slot does
+    nothing) through the C ABI."""
+    from test_oracle_pins import _KD_GOLDEN as fx, kpool_decode_golden_check, kpool_decode_golden_inputs
+
+    a = kpool_decode_golden_inputs(fx)
+    dev = "cuda"
+    t16 = lambda x: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+    cache = torch.from_numpy(a["cache"]).to(dev)
+    ring = t16(a["ring"])
+    err = torch.zeros((1,), dtype=torch.int32, device=dev)
+    ck.ckv_kpool_decode_update(cache, ring, torch.from_numpy(a["tail_slot_mapping"]).to(dev),
+                               torch.from_numpy(a["slot_mapping"]).to(dev), torch.from_numpy(a["positions"]).to(dev),
+                               t16(a["key"]), t16(a["score"]), torch.from_numpy(a["ape"]).to(dev), round_scale=True,
+                               err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    kpool_decode_golden_check(fx, u8(cache), bf16_bits(ring))
 
 
 def test_kpool_decode_bad_block_flags(ck):
@@ -404,6 +475,108 @@ def test_kpool_seed_tail_many_requests(ck, ora, P, misaligned):
     rring = bf16_bits(ring0).copy()
     ora.kpool_seed_tail(rring, bf16_bits(key), bf16_bits(score), tslot.numpy())
     np.testing.assert_array_equal(bf16_bits(ring), rring)
+
+
+@pytest.mark.parametrize("P", [4, 16])
+def test_kpool_prefill_seed_decode_continuity(ck, ora, P):
+    """Prefill -> decode on the pooled path (vLLM page kpool_compress:
+    kpool_compress_and_write_cache for the prefill's complete pools,
+    kpool_seed_tail_cache / _kpool_tail_seed_kernel for the ring, then
+    _kpool_decode_update_batched_kernel for the decode tokens).  The decode
+    tokens close the pool that straddles the prefill/decode boundary and the
+    next one.  Every cache row must equal the one-shot compression of that
+    pool's tokens taken straight from the whole sequence (staged FP8 checks),
+    and the ring must equal the oracle's after each step."""
+    B = 6
+    lens = [37, 16, 5, 64, 1, 50] if P == 16 else [9, 4, 2, 16, 1, 14]
+    N = 2 * P + 3
+    g = torch.Generator().manual_seed(60 + P)
+    seq_k = [torch.randn((n + N, D), generator=g).to(torch.bfloat16) for n in lens]
+    seq_s = [(torch.randn((n + N, D), generator=g) * 2).to(torch.bfloat16) for n in lens]
+    ape = torch.randn((P, D), generator=g) * 0.1
+    blocks = torch.randperm(B, generator=g)
+    cap = (max(lens) + N) // P + 1  # cache rows per request: row b * cap + pool index
+    ps = 16
+    pages = (B * cap + ps - 1) // ps
+    cache0 = torch.full((pages, ps, D + 4), 0x6B, dtype=torch.uint8)
+    ring0 = torch.randn((B, 2, P, D), generator=g).to(torch.bfloat16)  # stale contents
+    dev = "cuda"
+    cache, ring = cache0.to(dev), ring0.to(dev)
+    rcache, rring = u8(cache0).copy(), bf16_bits(ring0).copy()
+    err = torch.zeros((1,), dtype=torch.int32, device=dev)
+
+    # 1. the prefill's complete pools, one-shot
+    full = [(b, p) for b in range(B) for p in range(lens[b] // P)]
+    pk = torch.stack([seq_k[b][p * P:(p + 1) * P] for b, p in full])
+    pscore = torch.stack([seq_s[b][p * P:(p + 1) * P] for b, p in full])
+    ploc = torch.tensor([b * cap + p for b, p in full], dtype=torch.int64)
+    n1 = len(full)
+    tx1 = torch.zeros((n1, D), device=dev)
+    txb1 = torch.zeros((n1, D), dtype=torch.bfloat16, device=dev)
+    tyb1 = torch.zeros((n1, D), dtype=torch.bfloat16, device=dev)
+    ck.ckv_kpool_compress(pk.to(dev), pscore.to(dev), ape.to(dev), kv_cache=cache, loc=ploc.to(dev), tap_x=tx1,
+                          tap_xb=txb1, tap_yb=tyb1, err_word=err)
+    ora.kpool_compress(rcache, ps, bf16_bits(pk), bf16_bits(pscore), f32(ape), ploc.numpy())
+
+    # 2. the ring seeded from the prefill batch (requests back to back)
+    tslot = torch.cat([blocks[b] * P + torch.arange(n) % P for b, n in enumerate(lens)]).to(torch.int32)
+    pre_k = torch.cat([seq_k[b][:n] for b, n in enumerate(lens)])
+    pre_s = torch.cat([seq_s[b][:n] for b, n in enumerate(lens)])
+    ck.ckv_kpool_seed_tail(ring, pre_k.to(dev), pre_s.to(dev), tslot.to(dev), err_word=err)
+    ora.kpool_seed_tail(rring, bf16_bits(pre_k), bf16_bits(pre_s), tslot.numpy())
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bf16_bits(ring), rring, err_msg="ring after the seed")
+
+    # 3. N decode tokens per request in two calls
+    taps = []
+    for a, b_ in ((0, P - 1), (P - 1, N)):
+        pos = torch.tensor([[lens[b] + t for t in range(a, b_)] for b in range(B)], dtype=torch.int64)
+        ts = (blocks[:, None] * P + pos % P).to(torch.int32)
+        sm = torch.where(pos % P == P - 1, torch.arange(B)[:, None] * cap + pos // P, -1).to(torch.int32)
+        key = torch.stack([seq_k[b][lens[b] + a:lens[b] + b_] for b in range(B)])
+        score = torch.stack([seq_s[b][lens[b] + a:lens[b] + b_] for b in range(B)])
+        n_tok = B * (b_ - a)
+        tx = torch.full((n_tok, D), float("nan"), device=dev)
+        txb = torch.zeros((n_tok, D), dtype=torch.bfloat16, device=dev)
+        tyb = torch.zeros((n_tok, D), dtype=torch.bfloat16, device=dev)
+        ck.ckv_kpool_decode_update(cache, ring, ts.to(dev), sm.to(dev), pos.to(torch.int32).to(dev), key.to(dev),
+                                   score.to(dev), ape.to(dev), tap_x=tx, tap_xb=txb, tap_yb=tyb, err_word=err)
+        ora.kpool_decode_update(rcache, ps, rring, ts.numpy(), sm.numpy(), pos.to(torch.int32).numpy(),
+                                bf16_bits(key), bf16_bits(score), f32(ape))
+        flat_sm = sm.numpy().reshape(-1)
+        taps.append((tx, txb, tyb, np.nonzero(flat_sm >= 0)[0], flat_sm[flat_sm >= 0]))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    np.testing.assert_array_equal(bf16_bits(ring), rring, err_msg="ring after the decode calls")
+
+    # every complete pool of the whole sequence, one-shot from its own tokens
+    allp = [(b, p) for b in range(B) for p in range((lens[b] + N) // P)]
+    wk = torch.stack([seq_k[b][p * P:(p + 1) * P] for b, p in allp])
+    ws = torch.stack([seq_s[b][p * P:(p + 1) * P] for b, p in allp])
+    wloc = np.array([b * cap + p for b, p in allp], np.int64)
+    wcache = u8(cache0).copy()
+    ref = ora.kpool_compress(wcache, ps, bf16_bits(wk), bf16_bits(ws), f32(ape), wloc, taps=True)
+    assert sum(len(t[4]) for t in taps) == len(allp) - n1 and len(allp) - n1 >= 2 * B
+    # GPU rows in the order of allp: the prefill's pools, then the decode closings
+    gx = {int(l): r for l, r in zip(ploc.numpy(), f32(tx1))}
+    gxb = {int(l): r for l, r in zip(ploc.numpy(), bf16_bits(txb1))}
+    gyb = {int(l): r for l, r in zip(ploc.numpy(), bf16_bits(tyb1))}
+    for tx, txb, tyb, rows, locs in taps:
+        for r, l in zip(rows, locs):
+            gx[int(l)], gxb[int(l)], gyb[int(l)] = f32(tx)[r], bf16_bits(txb)[r], bf16_bits(tyb)[r]
+    gq, gs = cache_rows(u8(cache), ps, D, wloc)
+    rq, rs = cache_rows(wcache, ps, D, wloc)
+    ref["q"], ref["scale"] = rq, rs
+    check_rows(ora, np.stack([gx[int(l)] for l in wloc]), np.stack([gxb[int(l)] for l in wloc]),
+               np.stack([gyb[int(l)] for l in wloc]), gq, gs, ref, True, f"prefill-seed-decode P={P}")
+    # nothing but those rows was written
+    g = u8(cache).reshape(-1).copy()
+    for l in wloc:
+        page, tok = divmod(int(l), ps)
+        base = page * ps * (D + 4)
+        g[base + tok * D: base + tok * D + D] = 0x6B
+        g[base + ps * D + 4 * tok: base + ps * D + 4 * tok + 4] = 0x6B
+    assert np.all(g == 0x6B)
 
 
 # ------------------------------------------------- pool -> token expansion
