@@ -813,11 +813,14 @@ def rotation_timings(case, replays=100, warmup=20, round_scale=True):
                                        d["positions"], d["key"], d["score"], d["ape"], round_scale=round_scale,
                                        use_pdl=pdl, err_word=err)
     elif case.startswith("latency_floor"):
-        # same instance count as the pooled decode's cold timing
+        # same instance count as the pooled decode's cold timing; latency_floor<h>
+        # or latency_floor<h>_w<warps>_c<warps per CTA> (default 512 warps, 4 per CTA)
         nbytes = kpool_decode_bytes(synth.pooled_decode("cpu", seed=100))[0]
         R = max(2, math.ceil(4 * l2 / nbytes))
-        hops = int(case[-1])
-        n = 512
+        parts = case[len("latency_floor"):].split("_")
+        hops = int(parts[0])
+        n = next((int(p[1:]) for p in parts[1:] if p.startswith("w")), 512)
+        wpc = next((int(p[1:]) for p in parts[1:] if p.startswith("c")), 4)
         g = torch.Generator(device=dev)
         g.manual_seed(7)
 
@@ -827,7 +830,7 @@ def rotation_timings(case, replays=100, warmup=20, round_scale=True):
                     "out": torch.zeros((n, 256), device=dev, dtype=torch.uint8)}
 
         def call(d, pdl):
-            ck.ckv_latency_probe(hops, n, d["idx"], d["rows"], d["out"], warps_per_cta=4, use_pdl=pdl)
+            ck.ckv_latency_probe(hops, n, d["idx"], d["rows"], d["out"], warps_per_cta=wpc, use_pdl=pdl)
 
         nbytes = n * 4 + (n * 512 if hops == 2 else n * 4 if hops == 1 else 0)
     else:
