@@ -305,48 +305,160 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 1)
   }
 }
 
-// Decode / verify update: warp w of CTA c handles request c*kDecodeCtaWarps + w
-// and walks its N tokens in order (small CTAs spread a decode batch over all
-// SMs).  The index triples and key/score rows of kPrefetch tokens
-// are loaded together before they are processed one by one, so the only
-// dependent global round trip per group is a closing pool's ring read.  That
-// read uses ordinary (coherent) loads: the same lane stashed any of those slots
-// earlier in this call, so program order makes its stores visible.
+// Decode / verify update: one CTA of two warps per request, thread t owning
+// channels 2t and 2t + 1 of the pooled key (one bf16 pair: every row access
+// is a 4-byte access per thread, 256 B per CTA).  The request's tokens are
+// walked in order, kPrefetch at a time; all 64 threads load the group's index
+// words (the same words: broadcast) and their pair of the group's key and
+// score rows.  A closing pool's ring rows and bias are loaded together (the
+// one round trip that depends on the index words); its arithmetic is
+// deferred until the stashes of the later tokens of the group (or, after the
+// last group, of the request) have been issued, so those stores are not left
+// at the end of the critical path.  A thread's later store to a ring slot
+// cannot overtake its own earlier load of it (same thread, same address), and
+// the pool takes its current token from registers, so deferring is safe.  The
+// arithmetic per channel is that of the one-shot kernels (same operations,
+// same order), so both give identical rows.  A request's branch decisions
+// come from words both warps read alike, so the barrier inside a pool's
+// rotation is reached by the whole CTA.
 constexpr int kPrefetch = 4;
-constexpr int kDecodeCtaWarps = 4;  // measured: 8 -> 5.84 us, 4 -> 5.41 us, 2 -> 5.86 us per call
+constexpr int kDecThreads = kD / 2;  // two channels per thread
+
+// bf16 -> Hadamard-128 -> bf16 -> absmax FP8 of a 128-channel vector held as
+// channel pairs (2t, 2t + 1) by the 64 threads of a CTA.  Butterfly spans 1
+// (inside the thread), 2..32 (lane shuffles), 64 (the other warp, through
+// shared memory), each (u + v, u - v) in fp32, then one multiply by
+// fp32(1/sqrt(128)): the rotation of rotate_quantize, element for element.
+// After the one exchange each thread also forms the last stage of its
+// partner's pair, so every warp holds all 128 outputs (4 per lane) and the
+// absmax needs no second exchange.  Every thread of the CTA must call it.
+template <bool kRound>
+__device__ __forceinline__ void rotate_quantize_pair(float x0, float x1, int t, float2* s_x, uint32_t& codes,
+                                                     float& scale, float (&xb)[2], float (&yb)[2]) {
+  const int lane = t & 31;
+  xb[0] = round_bf16(x0);
+  xb[1] = round_bf16(x1);
+  float a0 = xb[0] + xb[1];  // span 1
+  float a1 = xb[0] - xb[1];
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {  // spans 2..32: partner lane l ^ m
+    // lower channel: a + o; upper channel: o - a, rounded once like a subtraction
+    const float o0 = __shfl_xor_sync(0xFFFFFFFFu, a0, m);
+    const float o1 = __shfl_xor_sync(0xFFFFFFFFu, a1, m);
+    const float sgn = (lane & m) ? -1.f : 1.f;
+    a0 = fmaf(a0, sgn, o0);
+    a1 = fmaf(a1, sgn, o1);
+  }
+  s_x[t] = make_float2(a0, a1);  // span 64: the pair of thread t ^ 32
+  __syncthreads();
+  const float2 p = s_x[t ^ 32];
+  float f0, f1, g0, g1;  // this thread's outputs, and its partner's
+  if (t < 32) {
+    f0 = a0 + p.x, f1 = a1 + p.y, g0 = a0 - p.x, g1 = a1 - p.y;
+  } else {
+    f0 = p.x - a0, f1 = p.y - a1, g0 = p.x + a0, g1 = p.y + a1;
+  }
+  const float c = __uint_as_float(0x3DB504F3u);  // fp32(1/sqrt(128))
+  yb[0] = round_bf16(f0 * c);
+  yb[1] = round_bf16(f1 * c);
+  float am = fmaxf(fmaxf(fabsf(yb[0]), fabsf(yb[1])), fmaxf(fabsf(round_bf16(g0 * c)), fabsf(round_bf16(g1 * c))));
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, m));
+  am = fmaxf(am, 1e-4f);
+  const float v = am * __uint_as_float(0x3B124925u);  // absmax * fp32(1/448)
+  float q0, q1;
+  if (kRound) {
+    // smallest power of two >= v; its exact reciprocal gives the IEEE quotient
+    const uint32_t bits = __float_as_uint(v);
+    const uint32_t e = (bits & 0x007FFFFFu) ? (bits & 0x7F800000u) + 0x00800000u : (bits & 0x7F800000u);
+    scale = __uint_as_float(e);
+    const float inv = __uint_as_float((254u << 23) - e);
+    q0 = fminf(fmaxf(yb[0] * inv, -448.f), 448.f);
+    q1 = fminf(fmaxf(yb[1] * inv, -448.f), 448.f);
+  } else {
+    scale = v;
+    q0 = fminf(fmaxf(__fdiv_rn(yb[0], scale), -448.f), 448.f);
+    q1 = fminf(fmaxf(__fdiv_rn(yb[1], scale), -448.f), 448.f);
+  }
+  codes = __nv_cvt_float2_to_fp8x2(make_float2(q0, q1), __NV_SATFINITE, __NV_E4M3) & 0xFFFFu;
+}
 
 template <int P, bool kRound>
-__global__ void __launch_bounds__(kDecodeCtaWarps * 32)
+__global__ void __launch_bounds__(kDecThreads)
     kpool_decode_kernel(const __grid_constant__ KpoolDecodeArgs a) {
-  __shared__ __align__(16) float s_ape[P * kD];
+  __shared__ float2 s_x[kDecThreads];
   pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x * kDecodeCtaWarps + (threadIdx.x >> 5);
-  const bool active = b < a.B;
+  const int t = threadIdx.x;
+  const int b = blockIdx.x;
   const int64_t cache_rows = a.num_pages * a.page_size;
+  const uint16_t* key = a.key + b * a.key_sb + 2 * t;
+  const uint16_t* score = a.score + b * a.score_sb + 2 * t;
 
   int32_t loc[kPrefetch], pos[kPrefetch], tslot[kPrefetch];
-  uint2 kc[kPrefetch], sc[kPrefetch];
+  uint32_t kc[kPrefetch], sc[kPrefetch];  // bf16 pairs of this thread's channels
   auto load_group = [&](int t0) {
 #pragma unroll
     for (int i = 0; i < kPrefetch; ++i) {
-      const int t = t0 + i;
-      if (t < a.N) {
-        const int64_t idx = static_cast<int64_t>(b) * a.N + t;
-        loc[i] = a.slot_mapping[idx];
-        pos[i] = a.positions[idx];
-        tslot[i] = a.tail_slot_mapping[idx];
-        kc[i] = ld_stream_u2(a.key + b * a.key_sb + t * a.key_st + 4 * lane);
-        sc[i] = ld_stream_u2(a.score + b * a.score_sb + t * a.score_st + 4 * lane);
+      const int tk = t0 + i;
+      if (tk < a.N) {
+        const int64_t idx = static_cast<int64_t>(b) * a.N + tk;
+        loc[i] = __ldg(a.slot_mapping + idx);
+        pos[i] = __ldg(a.positions + idx);
+        tslot[i] = __ldg(a.tail_slot_mapping + idx);
+        kc[i] = __ldg(reinterpret_cast<const uint32_t*>(key + tk * a.key_st));
+        sc[i] = __ldg(reinterpret_cast<const uint32_t*>(score + tk * a.score_st));
       } else {
         loc[i] = pos[i] = tslot[i] = -1;  // past N: neither closes nor stashes
-        kc[i] = sc[i] = make_uint2(0u, 0u);
+        kc[i] = sc[i] = 0u;
       }
     }
   };
-  if (active) load_group(0);  // in flight while the bias is staged
-  stage_ape<P>(s_ape, a.ape);
-  if (!active) return;
+  load_group(0);
+  pdl_trigger();
+
+  // the pool waiting for its arithmetic: its rows, bias, cache row and tap row
+  bool pend = false;
+  int64_t pend_loc = 0, pend_row = 0;
+  uint32_t kr[P], sr[P];
+  float2 ap[P];
+  auto finish = [&]() {
+    const uint64_t log2e2 = f2_pack(kLog2e, kLog2e);
+    uint64_t z[P];
+    float m0 = kNegBig, m1 = kNegBig;
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+      z[j] = f2_fma(f2_from_bf16x2(sr[j]), log2e2, f2_pack(ap[j].x * kLog2e, ap[j].y * kLog2e));
+      float z0, z1;
+      f2_unpack(z[j], z0, z1);
+      m0 = fmaxf(m0, z0);
+      m1 = fmaxf(m1, z1);
+    }
+    const uint64_t mm = f2_pack(m0, m1);
+    uint64_t den = f2_pack(0.f, 0.f), acc = den;
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+      float t0, t1;
+      f2_unpack(f2_sub(z[j], mm), t0, t1);
+      const uint64_t e = f2_pack(fast_exp2(t0), fast_exp2(t1));
+      den = f2_add(den, e);
+      acc = f2_fma(e, f2_from_bf16x2(kr[j]), acc);
+    }
+    float d0, d1, a0, a1;
+    f2_unpack(den, d0, d1);
+    f2_unpack(acc, a0, a1);
+    const float x0 = __fdividef(a0, d0), x1 = __fdividef(a1, d1);  // den in [1, P]
+    float xb[2], yb[2], scale;
+    uint32_t codes;
+    rotate_quantize_pair<kRound>(x0, x1, t, s_x, codes, scale, xb, yb);
+    const int64_t page = pend_loc / a.page_size, tok = pend_loc - page * a.page_size;
+    uint8_t* base = a.cache + page * a.page_size * kRowBytes;
+    reinterpret_cast<uint16_t*>(base + tok * kD)[t] = static_cast<uint16_t>(codes);
+    if (t == 0) *reinterpret_cast<float*>(base + a.page_size * kD + 4 * tok) = scale;
+    if (a.tap_x) reinterpret_cast<float2*>(a.tap_x + pend_row * kD)[t] = make_float2(x0, x1);
+    if (a.tap_xb) reinterpret_cast<uint32_t*>(a.tap_xb + pend_row * kD)[t] = pack_bf16x2_rn(xb[0], xb[1]);
+    if (a.tap_yb) reinterpret_cast<uint32_t*>(a.tap_yb + pend_row * kD)[t] = pack_bf16x2_rn(yb[0], yb[1]);
+    pend = false;
+  };
 
   for (int t0 = 0; t0 < a.N; t0 += kPrefetch) {
     if (t0 > 0) load_group(t0);
@@ -359,37 +471,37 @@ __global__ void __launch_bounds__(kDecodeCtaWarps * 32)
       if (!closes && !stash_valid) continue;
       const int64_t block = static_cast<int64_t>(max(tslot[i], 0)) / P;
       if (block >= a.num_blocks) {
-        if (lane == 0) flag_error(a.err, CKV_DEVERR_TAIL_BLOCK);
+        if (t == 0) flag_error(a.err, CKV_DEVERR_TAIL_BLOCK);
         continue;
       }
-      uint16_t* kring = a.ring + block * 2 * P * kD;
-      uint16_t* sring = kring + P * kD;
+      uint32_t* kring = reinterpret_cast<uint32_t*>(a.ring + block * 2 * P * kD) + t;
+      uint32_t* sring = kring + P * kD / 2;
       if (closes) {
         if (loc[i] >= cache_rows) {
-          if (lane == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
+          if (t == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
         } else {
-          uint2 kr[P], sr[P];
+          if (pend) finish();  // an earlier pool of this call (P < N): its registers are needed
 #pragma unroll
           for (int j = 0; j < P - 1; ++j) {
-            kr[j] = *reinterpret_cast<const uint2*>(kring + j * kD + 4 * lane);
-            sr[j] = *reinterpret_cast<const uint2*>(sring + j * kD + 4 * lane);
+            kr[j] = kring[j * (kD / 2)];
+            sr[j] = sring[j * (kD / 2)];
           }
           kr[P - 1] = kc[i];
           sr[P - 1] = sc[i];
-          float x[4], xb[4], yb[4], scale;
-          uint32_t codes;
-          pool_softmax<P>(kr, sr, s_ape, lane, x);
-          rotate_quantize<kRound>(x, lane, codes, scale, xb, yb);
-          cache_write(a.cache, a.page_size, loc[i], lane, codes, scale);
-          write_taps(a.tap_x, a.tap_xb, a.tap_yb, static_cast<int64_t>(b) * a.N + t0 + i, lane, x, xb, yb);
+#pragma unroll
+          for (int j = 0; j < P; ++j) ap[j] = __ldg(reinterpret_cast<const float2*>(a.ape + j * kD) + t);
+          pend = true;
+          pend_loc = loc[i];
+          pend_row = static_cast<int64_t>(b) * a.N + t0 + i;
         }
       }
       if (stash_valid) {
-        *reinterpret_cast<uint2*>(kring + slot * kD + 4 * lane) = kc[i];
-        *reinterpret_cast<uint2*>(sring + slot * kD + 4 * lane) = sc[i];
+        kring[slot * (kD / 2)] = kc[i];
+        sring[slot * (kD / 2)] = sc[i];
       }
     }
   }
+  if (pend) finish();
 }
 
 // Tail-ring seed: each warp takes 128 consecutive prefill tokens, 4 per lane.
@@ -544,10 +656,9 @@ cudaError_t compress_p(const KpoolCompressArgs& a, bool round_scale, bool use_pd
 
 template <int P>
 cudaError_t decode_p(const KpoolDecodeArgs& a, bool round_scale, bool use_pdl, cudaStream_t s) {
-  const dim3 grid((a.B + kDecodeCtaWarps - 1) / kDecodeCtaWarps);
-  return round_scale
-             ? launch_ex(kpool_decode_kernel<P, true>, grid, dim3(kDecodeCtaWarps * 32), 0, use_pdl, s, a)
-             : launch_ex(kpool_decode_kernel<P, false>, grid, dim3(kDecodeCtaWarps * 32), 0, use_pdl, s, a);
+  const dim3 grid(static_cast<unsigned>(a.B));
+  return round_scale ? launch_ex(kpool_decode_kernel<P, true>, grid, dim3(kDecThreads), 0, use_pdl, s, a)
+                     : launch_ex(kpool_decode_kernel<P, false>, grid, dim3(kDecThreads), 0, use_pdl, s, a);
 }
 
 template <int P>
