@@ -59,7 +59,7 @@ WORKLOAD = ("serving step: pooled decode/verify B=512 N=4 P=16 D=128 + c128 deco
 NCU_TRAFFIC = {
     "c128_online_prefill_bf16": {"bytes_per_launch": 2172.4e6, "files": ["prefill_tma.cu", "ckv_tma.cuh", "ckv_fp8.cuh",
                                                                          "ckv_device.cuh"],
-                                 "src": "e0e51d0743e62e33"},
+                                 "src": "20a3853b5c6fbcd6"},
 }
 
 
@@ -1010,6 +1010,32 @@ def main():
             stream.synchronize()
         _barrier(ws)
         elapsed_ms = e_start.elapsed_time(e_end)
+
+        def run_steps(skip):
+            """K steps launched exactly like the timed region, without call `skip`."""
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e_d = torch.cuda.Event()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            dstream.wait_event(e0)
+            for _ in range(K):
+                with torch.cuda.stream(dstream):
+                    for i in (0, 1):
+                        if i != skip:
+                            step.call(i, pdl)
+                for i in range(2, nk):
+                    if i != skip:
+                        step.call(i, pdl)
+            e_d.record(dstream)
+            stream.wait_event(e_d)
+            e1.record(stream)
+            stream.synchronize()
+            return e0.elapsed_time(e1)
+
+        # what each call adds to the launched step: the step's time minus the time
+        # of the same step without that call (overlap and launch chaining included)
+        full_again_ms = run_steps(None)
+        marginal_ms = [(full_again_ms - run_steps(i)) / K for i in range(nk)]
         # breakdown: the same steps with an event between consecutive calls (an event
         # between two launches removes the programmatic overlap, so this loop is
         # timed on its own and used only to attribute time to the five calls).
@@ -1039,7 +1065,11 @@ def main():
     for i, n in enumerate(step.names):
         gbs = step.bytes[i] / (per_kernel_ms[i] / 1e3) / 1e9
         kernels[n] = {"us": round(per_kernel_ms[i] * 1e3, 2), "bytes": int(step.bytes[i]), "gbs": round(gbs, 1),
-                      "frac_of_" + peak_kind + "_peak": round(gbs / peak, 4), "tokens": int(step.tokens[i]),
+                      "frac_of_" + peak_kind + "_peak": round(gbs / peak, 4),
+                      "us_in_step_marginal": round(marginal_ms[i] * 1e3, 2),
+                      "frac_in_step_marginal": (round(step.bytes[i] / (marginal_ms[i] / 1e3) / 1e9 / peak, 4)
+                                                if marginal_ms[i] > 0 else None),
+                      "tokens": int(step.tokens[i]),
                       "compressed_rows": int(step.rows[i]),
                       "tokens_per_s": round(step.tokens[i] / (per_kernel_ms[i] / 1e3), 1)}
     kernels["kpool_decode_update_linear_scale"] = {
@@ -1142,7 +1172,13 @@ def main():
             "launch_chaining": ("programmatic dependent launch" if pdl else "stream order") +
                                ("; decode calls on a second stream, concurrent with the prefill calls"
                                 if overlap else "; one stream"),
-            "breakdown_ms_per_step": round(breakdown_ms, 4), "kernels": kernels, "roofline": roofline, "clocks": clk.summary(),
+            "breakdown_ms_per_step": round(breakdown_ms, 4),
+            "per_call_timing": ("us / frac_of_*_peak: an event pair around each call in stream order (each event "
+                                "breaks the launch chaining, so every call also pays a launch gap); "
+                                "us_in_step_marginal: the chained step's time minus the same step's time without "
+                                "that call (calls on the decode stream overlap the prefill stream, so theirs is "
+                                "near zero)"),
+            "kernels": kernels, "roofline": roofline, "clocks": clk.summary(),
             "gpu_launches": step.launches() * K, "e2e": e2e, "cpu_baseline": cpu, "decode_l2_cold": decode_cold,
         }), flush=True)
     if ws > 1:
