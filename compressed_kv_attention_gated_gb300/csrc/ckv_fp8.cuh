@@ -11,6 +11,15 @@
 
 namespace ckv {
 
+// Largest of the 32 lanes' non-negative values in one warp reduction: a
+// non-negative float orders like its bit pattern, so the unsigned max of the
+// bits is the float max (exact).  A NaN counts as 0, as fmaxf ignores it.
+__device__ __forceinline__ float warp_absmax(float am) {
+  uint32_t u = __float_as_uint(am);
+  u = u > 0x7F800000u ? 0u : u;
+  return __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, u));
+}
+
 // x (fp32) -> bf16 -> Hadamard-128 (fp32) -> bf16 -> absmax FP8-e4m3 + scale.
 // The rotation is the orthonormal Sylvester Hadamard matrix: butterfly spans
 // 1, 2, 4, ..., 64 in ascending order, each (u + v, u - v) in fp32, then one
@@ -56,8 +65,7 @@ __device__ __forceinline__ void rotate_quantize(const float (&x)[4], int lane, u
     yb[i] = round_bf16(a[i] * c);
     am = fmaxf(am, fabsf(yb[i]));
   }
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, m));
+  am = warp_absmax(am);
   am = fmaxf(am, 1e-4f);
   const float v = am * __uint_as_float(0x3B124925u);  // absmax * fp32(1/448)
   float q[4];

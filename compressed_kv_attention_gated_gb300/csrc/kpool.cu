@@ -18,8 +18,9 @@
 //     bulk copies (cp.async.bulk, completion on an mbarrier), so the next
 //     pool's 8 KB arrive while the current one is reduced, rotated and packed;
 //   * Hadamard-128: two butterfly spans inside the lane (1, 2), then five
-//     warp-shuffle spans (4..64 = lane masks 1..16), ascending; warp-shuffle
-//     absmax; fused FP8-e4m3 packing (cvt.rn.satfinite) and cache write.
+//     warp-shuffle spans (4..64 = lane masks 1..16), ascending; the absmax as
+//     one warp max-reduction of the values' bit patterns; fused FP8-e4m3
+//     packing (cvt.rn.satfinite) and cache write.
 //
 // The pooled path is memory bound (no dense contraction); no tensor cores.
 #include "ckv_device.cuh"
@@ -331,7 +332,8 @@ constexpr int kDecThreads = kD / 2;  // two channels per thread
 // fp32(1/sqrt(128)): the rotation of rotate_quantize, element for element.
 // After the one exchange each thread also forms the last stage of its
 // partner's pair, so every warp holds all 128 outputs (4 per lane) and the
-// absmax needs no second exchange.  Every thread of the CTA must call it.
+// absmax is one warp reduction, with no second exchange.  Every thread of the
+// CTA must call it.
 template <bool kRound>
 __device__ __forceinline__ void rotate_quantize_pair(float x0, float x1, int t, float2* s_x, uint32_t& codes,
                                                      float& scale, float (&xb)[2], float (&yb)[2]) {
@@ -362,9 +364,7 @@ __device__ __forceinline__ void rotate_quantize_pair(float x0, float x1, int t, 
   yb[0] = round_bf16(f0 * c);
   yb[1] = round_bf16(f1 * c);
   float am = fmaxf(fmaxf(fabsf(yb[0]), fabsf(yb[1])), fmaxf(fabsf(round_bf16(g0 * c)), fabsf(round_bf16(g1 * c))));
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, m));
-  am = fmaxf(am, 1e-4f);
+  am = fmaxf(warp_absmax(am), 1e-4f);
   const float v = am * __uint_as_float(0x3B124925u);  // absmax * fp32(1/448)
   float q0, q1;
   if (kRound) {
