@@ -735,14 +735,22 @@ def run_case(args):
 def run_rotation(args):
     """--case c128_decode|kpool_decode|latency_floor0|1|2 --rotate: print
     rotation_timings() as one JSON line."""
-    print(json.dumps(rotation_timings(args.case, args.steps, args.warmup, round_scale=not args.linear_scale)))
+    print(json.dumps(rotation_timings(args.case, args.steps, args.warmup, round_scale=not args.linear_scale,
+                                      instances=args.instances)))
 
 
-def rotation_timings(case, replays=100, warmup=20, round_scale=True):
+# Instances of a decode batch in one cold-timing graph, at least: the graph's
+# own launch cost is spread over its calls, and with 17 calls (enough for 4 x
+# L2 of the c128 decode) it still added a few percent to each.
+kMinInstances = 64
+
+
+def rotation_timings(case, replays=100, warmup=20, round_scale=True, instances=None):
     """Decode calls timed L2-cold and warm, each replayed from one CUDA graph.
 
     Cold: R independent instances of the batch (R x algorithmic bytes >= 4 x
-    the L2 size), one call on each, captured in order as one graph; every
+    the L2 size, and R >= kMinInstances), one call on each, captured in order
+    as one graph; every
     replay is bracketed by events and the median replay time / R is the time of
     one call that finds none of its data in L2.  Warm: a graph of one call on
     one instance (its data L2-resident after the first replay).  Both with and
@@ -763,7 +771,11 @@ def rotation_timings(case, replays=100, warmup=20, round_scale=True):
     latency_floor: the ckv_latency_probe kernels (0, 1 and 2 dependent global
     round trips per warp) in the pooled decode's launch shape, R instances of
     512 warps with an L2 flush before every replay: the floor under the pooled
-    decode's cold time."""
+    decode's cold time.  latency_floor<h>_r<rows> draws the second hop's rows
+    from a buffer of <rows> x 256 B (default 512 rows).
+
+    instances: a fixed instance count instead of the L2-sized one, with an L2
+    flush before every replay (data cold, the instances' pages recently used)."""
     import math
 
     import compressed_kv_attention_gated_gb300 as ck
@@ -779,7 +791,7 @@ def rotation_timings(case, replays=100, warmup=20, round_scale=True):
     if case == "c128_decode":
         first = synth.c128_decode(dev, seed=100)
         nbytes = c128_decode_bytes(first)[0]
-        R = max(2, math.ceil(4 * l2 / nbytes))
+        R = max(kMinInstances, math.ceil(4 * l2 / nbytes))
 
         def make(r):
             d = first if r == 0 else synth.c128_decode(dev, seed=100 + r)
@@ -797,7 +809,7 @@ def rotation_timings(case, replays=100, warmup=20, round_scale=True):
         first = synth.pooled_decode(dev, seed=100)
         nbytes = kpool_decode_bytes(first)[0]
         B, ps = first["B"], first["page_size"]
-        R = max(2, math.ceil(4 * l2 / nbytes))
+        R = max(kMinInstances, math.ceil(4 * l2 / nbytes))
         cache = torch.zeros(((R * B + ps - 1) // ps, ps, first["D"] + 4), device=dev, dtype=torch.uint8)
 
         def make(r):
@@ -816,17 +828,18 @@ def rotation_timings(case, replays=100, warmup=20, round_scale=True):
         # same instance count as the pooled decode's cold timing; latency_floor<h>
         # or latency_floor<h>_w<warps>_c<warps per CTA> (default 512 warps, 4 per CTA)
         nbytes = kpool_decode_bytes(synth.pooled_decode("cpu", seed=100))[0]
-        R = max(2, math.ceil(4 * l2 / nbytes))
+        R = max(kMinInstances, math.ceil(4 * l2 / nbytes))
         parts = case[len("latency_floor"):].split("_")
         hops = int(parts[0])
         n = next((int(p[1:]) for p in parts[1:] if p.startswith("w")), 512)
         wpc = next((int(p[1:]) for p in parts[1:] if p.startswith("c")), 4)
+        nrows = next((int(p[1:]) for p in parts[1:] if p.startswith("r")), n)
         g = torch.Generator(device=dev)
         g.manual_seed(7)
 
         def make(r):
-            return {"idx": torch.randperm(n, generator=g, device=dev).to(torch.int32),
-                    "rows": torch.randint(0, 255, (n, 256), generator=g, device=dev, dtype=torch.uint8),
+            return {"idx": torch.randperm(nrows, generator=g, device=dev)[:n].to(torch.int32),
+                    "rows": torch.randint(0, 255, (nrows, 256), generator=g, device=dev, dtype=torch.uint8),
                     "out": torch.zeros((n, 256), device=dev, dtype=torch.uint8)}
 
         def call(d, pdl):
@@ -835,8 +848,10 @@ def rotation_timings(case, replays=100, warmup=20, round_scale=True):
         nbytes = n * 4 + (n * 512 if hops == 2 else n * 4 if hops == 1 else 0)
     else:
         raise SystemExit("--rotate applies to --case c128_decode, kpool_decode or latency_floor0|1|2")
+    if instances:
+        R = int(instances)
     inst = [make(r) for r in range(R)]
-    flush_each = restore is not None or case.startswith("latency_floor")
+    flush_each = restore is not None or case.startswith("latency_floor") or bool(instances)
     peak, peak_kind = _peaks()
     stream = torch.cuda.Stream(dev)
     res = {"case": case, "mode": "rotate", "instances": R, "l2_bytes": l2, "bytes_per_call": nbytes,
@@ -928,6 +943,8 @@ def main():
                          "replays over rotating instances (--steps replays, median)")
     ap.add_argument("--linear-scale", action="store_true",
                     help="with --case kpool_decode --rotate: the linear FP8 scale instead of the power-of-two one")
+    ap.add_argument("--instances", type=int, default=None,
+                    help="with --rotate: this many instances, L2 flushed before every replay")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
@@ -1154,7 +1171,7 @@ def main():
             if "gbs_cold_physical" in r["pdl"]:
                 e["frac_physical"] = r["pdl"][f"frac_of_{peak_kind}_hbm_physical"]
             decode_cold[name] = e
-        decode_cold["method"] = ("R instances (R x bytes per call >= 4 x L2), one call on each, captured in order "
+        decode_cold["method"] = ("R instances (R x bytes per call >= 4 x L2, R >= 64), one call on each, captured in order "
                                  "in one CUDA graph with programmatic dependent launch; median of 100 replays / R. "
                                  "c128 decode: every state pool restored from a pristine copy and a 2 x L2 buffer "
                                  "written before each replay (outside the events). latency_floor: the probe "
