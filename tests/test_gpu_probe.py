@@ -1,0 +1,44 @@
+"""ckv_latency_probe: the latency-floor kernels behind the decode measurements
+do the memory work they claim.  Two hops: each warp copies the row its index
+names (out of range: the warp writes nothing); one hop: each warp writes its
+index word to the first 4 bytes of its output row; zero hops: nothing."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ck():
+    import compressed_kv_attention_gated_gb300 as ck
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ck.load()
+    return ck
+
+
+@pytest.mark.parametrize("warps_per_cta", [1, 4, 32])
+def test_probe_hops_copy_what_they_claim(ck, warps_per_cta):
+    g = torch.Generator().manual_seed(warps_per_cta)
+    n, nrows = 777, 4096
+    idx = torch.randperm(nrows, generator=g)[:n].to(torch.int32)
+    idx[5], idx[9] = -1, nrows  # skipped by the second hop
+    rows = torch.randint(0, 256, (nrows, 256), generator=g, dtype=torch.uint8)
+    dev = "cuda"
+    d_idx, d_rows = idx.to(dev), rows.to(dev)
+    out2 = torch.full((n, 256), 0xEE, dtype=torch.uint8, device=dev)
+    out1 = torch.full((n, 256), 0xEE, dtype=torch.uint8, device=dev)
+    out0 = torch.full((n, 256), 0xEE, dtype=torch.uint8, device=dev)
+    ck.ckv_latency_probe(2, n, d_idx, d_rows, out2, warps_per_cta=warps_per_cta, use_pdl=True)
+    ck.ckv_latency_probe(1, n, d_idx, d_rows, out1, warps_per_cta=warps_per_cta)
+    ck.ckv_latency_probe(0, n, d_idx, d_rows, out0, warps_per_cta=warps_per_cta)
+    torch.cuda.synchronize()
+    o2, o1, o0 = out2.cpu().numpy(), out1.cpu().numpy(), out0.cpu().numpy()
+    ok = (idx >= 0) & (idx < nrows)
+    np.testing.assert_array_equal(o2[ok.numpy()], rows.numpy()[idx[ok].numpy()])
+    assert np.all(o2[~ok.numpy()] == 0xEE)
+    np.testing.assert_array_equal(o1[:, :4].copy().view(np.int32)[:, 0], idx.numpy())
+    assert np.all(o1[:, 4:] == 0xEE)
+    assert np.all(o0 == 0xEE)
