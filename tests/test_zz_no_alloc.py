@@ -106,3 +106,25 @@ def test_noalloc_rejects_oversize_range(ck):
     with pytest.raises(ck.CkvError) as e:
         _noalloc(ck, ids, MAX_RANGE + 1)
     assert e.value.status == 2
+
+
+@pytest.mark.gpu
+def test_noalloc_on_each_device(ck):
+    """The bitmap's device address is looked up per device: on every GPU of
+    the machine (one at a time, that device current) the allocation-free call
+    agrees with the scratch one.  With one GPU this is the first device only."""
+    n_dev = torch.cuda.device_count()
+    perm = np.random.default_rng(5).permutation(20000).astype(np.int64)
+    rep = perm.copy()
+    rep[-1] = rep[3]
+    for dev in range(n_dev):
+        with torch.cuda.device(dev):
+            for ids_np, want in ((perm, 0), (rep, DISTINCT)):
+                ids = torch.from_numpy(ids_np).to(f"cuda:{dev}")
+                na = torch.zeros((1,), dtype=torch.int32, device=f"cuda:{dev}")
+                ck.ckv_check_distinct_noalloc(ids, 20000, na)
+                sa = torch.zeros((1,), dtype=torch.int32, device=f"cuda:{dev}")
+                scratch = torch.full(((20000 + 31) // 32,), -1, dtype=torch.int32, device=f"cuda:{dev}")
+                ck.ckv_check_distinct(ids, 20000, scratch, sa)
+                torch.cuda.synchronize(dev)
+                assert int(na.item()) == int(sa.item()) == want, dev
