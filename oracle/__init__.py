@@ -47,11 +47,14 @@ def _p(a, ct):
 
 
 def lib():
+    """The oracle library: ``libckv_oracle.so`` built from ``ckv_oracle.cpp``,
+    or the build named by CKV_ORACLE_SO (the mutation tests point it at a copy
+    with a planted mistake, to show that the pins catch it)."""
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            L = ctypes.CDLL(_LIB)
+            path = os.environ.get("CKV_ORACLE_SO") or build()
+            L = ctypes.CDLL(path)
             P = ctypes.POINTER
             f32, f64, u8, u16, i32, i64, u32 = (ctypes.c_float, ctypes.c_double, ctypes.c_uint8,
                                                 ctypes.c_uint16, ctypes.c_int32, ctypes.c_int64,
