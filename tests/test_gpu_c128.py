@@ -256,6 +256,61 @@ def test_c128_prefill_full_size(variant, ck, ora, use_pdl, pad):
     assert nrows > 1000 and nstates > 30
 
 
+def test_c128_prefill_full_size_states_from_prior_tokens(ck, ora):
+    """Full size (64 requests, prefix U[0,16384], extend U[1,8192], D=512 fp32)
+    with each request's slot holding the state of its prefix's last, partial
+    chunk: p = prefix % 128 virtual prior tokens drawn like the input
+    (synth.prior_chunk_tokens), reduced by the oracle's two-pass.  Every
+    compressed row must then equal a two-pass over all 128 tokens of its chunk
+    (the prior ones included for the first chunk) and every new state the
+    two-pass over its chunk's tokens (sglang page c128_online.cuh,
+    flash_c128_online_prefill; consistent initial states)."""
+    from compressed_kv_attention_gated_gb300 import synth
+
+    d = synth.c128_prefill("cpu", seed=12)
+    D, B = d["D"], d["B"]
+    seq = d["seq_lens"].numpy().astype(np.int64)
+    ext = d["extend_lens"].numpy().astype(np.int64)
+    prefix = seq - ext
+    prior, p = synth.prior_chunk_tokens(torch.from_numpy(prefix + 1), D, seed=13)
+    p = p.numpy()
+    assert np.array_equal(p, prefix % 128) and (p > 0).sum() > 50
+    ape = f32(d["ape"])
+    idx = d["indices"].numpy()
+    zeros = np.zeros((1, 3, D), np.float32)
+    has = p > 0
+    _, _, fs, sw = ora.c128_prefill(zeros, f32(prior), ape, np.zeros(int(has.sum()), np.int32), prefix[has],
+                                    p[has])
+    assert sw.all()
+    state = d["state"].clone()
+    state[torch.from_numpy(idx[has]).long()] = torch.from_numpy(fs.astype(np.float32))
+    d["state"] = state
+    g_state, g_out, err, _ = _prefill_gpu(ck, d, use_pdl=True)
+    assert err == 0
+    nrows, nstates = _check_prefill(ora, d, g_state, g_out)
+    assert nrows > 1000 and nstates > 30
+    # every request from the start of its prefix's last chunk, in one piece
+    pstart = np.concatenate([[0], np.cumsum(p)])
+    estart = np.concatenate([[0], np.cumsum(ext)])
+    inp = f32(d["input"])
+    full = np.concatenate([np.concatenate([f32(prior)[pstart[b]:pstart[b + 1]], inp[estart[b]:estart[b + 1]]])
+                           for b in range(B)])
+    out2, written2, fs2, sw2 = ora.c128_prefill(zeros, full, ape, np.zeros(B, np.int32), seq, p + ext)
+    fstart = np.concatenate([[0], np.cumsum(p + ext)])
+    # GPU ragged row estart[b] + i is row fstart[b] + p[b] + i of the whole-chunk layout
+    rows = np.concatenate([np.arange(ext[b]) + estart[b] for b in range(B)])
+    frows = np.concatenate([np.arange(ext[b]) + fstart[b] + p[b] for b in range(B)])
+    go = f32(g_out)
+    wr = written2[frows]
+    assert wr.sum() == nrows
+    assert_close_rel(go[rows[wr]], out2[frows[wr]], "compressed rows vs two-pass over whole chunks")
+    gs = f32(g_state)
+    assert np.array_equal(sw2, ~((seq % 128) == 0))
+    assert_close_abs(gs[idx[sw2], 0], fs2[sw2, 0], what="max vs two-pass")
+    assert_close_rel(gs[idx[sw2], 1], fs2[sw2, 1], "sum vs two-pass")
+    assert_close_rel(gs[idx[sw2], 2], fs2[sw2, 2], "kv vs two-pass")
+
+
 # (prefix, extend) pairs on every chunk boundary: first token of a chunk,
 # last token of a chunk, exactly one chunk, one past it, single tokens, spans
 # of many chunks, and segments ending on position 127 with nothing to write
