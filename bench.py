@@ -772,7 +772,9 @@ def rotation_timings(case, replays=100, warmup=20, round_scale=True, instances=N
     round trips per warp) in the pooled decode's launch shape, R instances of
     512 warps with an L2 flush before every replay: the floor under the pooled
     decode's cold time.  latency_floor<h>_r<rows> draws the second hop's rows
-    from a buffer of <rows> x 256 B (default 512 rows).
+    from a buffer of <rows> x 256 B (default 512 rows); latency_floor3 is one
+    round trip with the pooled decode's own first-hop loads (512 warps or more,
+    9 rows or more).
 
     instances: a fixed instance count instead of the L2-sized one, with an L2
     flush before every replay (data cold, the instances' pages recently used)."""
@@ -845,7 +847,7 @@ def rotation_timings(case, replays=100, warmup=20, round_scale=True, instances=N
         def call(d, pdl):
             ck.ckv_latency_probe(hops, n, d["idx"], d["rows"], d["out"], warps_per_cta=wpc, use_pdl=pdl)
 
-        nbytes = n * 4 + (n * 512 if hops == 2 else n * 4 if hops == 1 else 0)
+        nbytes = {0: 0, 1: n * 8, 2: n * 516, 3: n * (48 + 1024 + 4)}[hops]
     else:
         raise SystemExit("--rotate applies to --case c128_decode, kpool_decode or latency_floor0|1|2")
     if instances:

@@ -600,8 +600,9 @@ def ckv_check_distinct_noalloc(ids, id_range, err_word, stream=None):
 
 def ckv_latency_probe(hops, n_warps, idx=None, rows=None, out=None, warps_per_cta=4, use_pdl=False, stream=None):
     """Latency floor of a decode-sized launch (see include/ckv.h): hops 0, 1 or
-    2 dependent global round trips per warp.  idx int32 [n_warps]; rows and out
-    uint8 [*, 256]; stream defaults to the current stream."""
+    2 dependent global round trips per warp, or 3 for one round trip with the
+    pooled decode's first-hop loads.  idx int32 [n_warps]; rows and out uint8
+    [*, 256]; stream defaults to the current stream."""
     L = load()
     _cuda("ckv_latency_probe", idx, rows, out)
     if idx is not None:

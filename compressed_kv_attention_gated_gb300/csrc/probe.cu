@@ -12,6 +12,11 @@
 //           global round trip;
 //   hops 2  each warp loads idx[w], then the 256-byte row rows[idx[w]] (8 bytes
 //           per lane), then stores that row: two dependent round trips.
+//   hops 3  one round trip carrying the pooled decode's first-hop loads: each
+//           thread loads 12 index words (idx[b0 .. b0 + 15], the same for the
+//           warp, b0 = w rounded down to a multiple of 4 and kept inside idx)
+//           and 8 four-byte row words 256 bytes apart, and lane 0 stores the
+//           exclusive or of the 20 words it loaded.
 // An index outside [0, num_rows) is skipped.
 #include <cstdint>
 
@@ -33,9 +38,20 @@ __global__ void latency_probe_kernel(const int32_t* idx, const uint2* rows, int6
     const int32_t r = idx[w];
     if constexpr (kHops == 1) {
       if (lane == 0) reinterpret_cast<int32_t*>(out + w * 32)[0] = r;
-    } else {
+    } else if constexpr (kHops == 2) {
       if (r < 0 || r >= num_rows) return;
       out[w * 32 + lane] = rows[static_cast<int64_t>(r) * 32 + lane];
+    } else {
+      // n_warps >= 16 and num_rows >= 9 (checked by the caller): the 16 index
+      // words and the 8 row words below stay inside idx and rows
+      const int64_t b0 = min(w & ~int64_t{3}, static_cast<int64_t>(n_warps) - 16);
+      int32_t acc = r;
+#pragma unroll
+      for (int q = 1; q < 12; ++q) acc ^= idx[b0 + ((q * 7) & 15)];
+      const uint32_t* rw = reinterpret_cast<const uint32_t*>(rows) + (w * 8) % (num_rows * 64 - 512) + lane;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc ^= static_cast<int32_t>(rw[q * 64]);
+      if (lane == 0) reinterpret_cast<int32_t*>(out + w * 32)[0] = acc;
     }
   }
 }
@@ -52,6 +68,7 @@ cudaError_t launch_latency_probe(int hops, const int32_t* idx, const void* rows,
     case 0: return launch_ex(latency_probe_kernel<0>, grid, block, 0, use_pdl, s, idx, r, num_rows, o, n_warps);
     case 1: return launch_ex(latency_probe_kernel<1>, grid, block, 0, use_pdl, s, idx, r, num_rows, o, n_warps);
     case 2: return launch_ex(latency_probe_kernel<2>, grid, block, 0, use_pdl, s, idx, r, num_rows, o, n_warps);
+    case 3: return launch_ex(latency_probe_kernel<3>, grid, block, 0, use_pdl, s, idx, r, num_rows, o, n_warps);
     default: return cudaErrorInvalidValue;
   }
 }

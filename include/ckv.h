@@ -455,12 +455,20 @@ ckv_status ckv_c128_online_prefill_counted_fp8(float* state, int64_t num_slots, 
  *   hops == 2  loads idx[w], then row idx[w] of rows, and stores it as row w
  *              of out (two dependent round trips, as when a closing pool's
  *              index words name the ring rows it reads).
+ *   hops == 3  one round trip with the pooled decode's first-hop loads: each
+ *              thread loads 12 words of idx[b0 .. b0 + 15] (b0 = w rounded
+ *              down to a multiple of 4, at most n_warps - 16) and 8 four-byte
+ *              words of rows 256 bytes apart, starting at word
+ *              (8w mod (64 num_rows - 512)) + lane; lane 0 stores the
+ *              exclusive or of the 20 words it loaded (idx[w] among them) to
+ *              the first 4 bytes of row w of out.  Needs n_warps >= 16 and
+ *              num_rows >= 9.
  *   idx        device int32 [n_warps] (hops >= 1); an index outside
- *              [0, num_rows) makes that warp skip its row
- *   rows       device [num_rows][256 bytes], 8-byte aligned (hops == 2)
+ *              [0, num_rows) makes that warp skip its row (hops == 2)
+ *   rows       device [num_rows][256 bytes], 8-byte aligned (hops >= 2)
  *   out        device [n_warps][256 bytes], 8-byte aligned (hops >= 1)
- * Sizes outside hops 0..2, n_warps >= 1, 1 <= warps_per_cta <= 32 return
- * CKV_ERR_SHAPE and launch nothing.
+ * Sizes outside hops 0..3, n_warps >= 1, 1 <= warps_per_cta <= 32 (and the
+ * hops == 3 minimums) return CKV_ERR_SHAPE and launch nothing.
  */
 ckv_status ckv_latency_probe(int32_t hops, const int32_t* idx, const void* rows, int64_t num_rows, void* out,
                              int32_t n_warps, int32_t warps_per_cta, int32_t use_pdl, void* stream);

@@ -1,7 +1,9 @@
 """ckv_latency_probe: the latency-floor kernels behind the decode measurements
 do the memory work they claim.  Two hops: each warp copies the row its index
 names (out of range: the warp writes nothing); one hop: each warp writes its
-index word to the first 4 bytes of its output row; zero hops: nothing."""
+index word to the first 4 bytes of its output row; the first-hop mode: lane
+0's exclusive or of the 12 index words and 8 row words it loaded; zero hops:
+nothing."""
 import numpy as np
 import pytest
 import torch
@@ -42,3 +44,29 @@ def test_probe_hops_copy_what_they_claim(ck, warps_per_cta):
     np.testing.assert_array_equal(o1[:, :4].copy().view(np.int32)[:, 0], idx.numpy())
     assert np.all(o1[:, 4:] == 0xEE)
     assert np.all(o0 == 0xEE)
+
+
+@pytest.mark.parametrize("n", [16, 1024, 777])
+def test_probe_first_hop_mode(ck, n):
+    g = torch.Generator().manual_seed(n)
+    nrows = 4096
+    idx = torch.randint(-2**31, 2**31 - 1, (n,), generator=g, dtype=torch.int64).to(torch.int32)
+    rows = torch.randint(0, 256, (nrows, 256), generator=g, dtype=torch.uint8)
+    out = torch.full((n, 256), 0xEE, dtype=torch.uint8, device="cuda")
+    ck.ckv_latency_probe(3, n, idx.cuda(), rows.cuda(), out, warps_per_cta=2, use_pdl=True)
+    torch.cuda.synchronize()
+    iw = idx.numpy()
+    rw = rows.numpy().view(np.uint32).reshape(-1)
+    want = np.empty(n, np.uint32)
+    for w in range(n):
+        b0 = min(w & ~3, n - 16)
+        acc = np.uint32(iw[w])
+        for q in range(1, 12):
+            acc ^= np.uint32(iw[b0 + ((q * 7) & 15)])
+        base = (w * 8) % (nrows * 64 - 512)  # lane 0's words: the ones it stores
+        for q in range(8):
+            acc ^= rw[base + q * 64]
+        want[w] = acc
+    o = out.cpu().numpy()
+    np.testing.assert_array_equal(o[:, :4].copy().view(np.uint32)[:, 0], want)
+    assert np.all(o[:, 4:] == 0xEE)
