@@ -2,9 +2,9 @@
 //
 // The pooled decode update is bound by latency, not bandwidth: one call moves
 // about 3 MB, and a closing pool needs two dependent global round trips (its
-// token's index words, then the ring rows they name).  These kernels have the
-// decode kernel's launch shape (one warp per request, a few warps per CTA) and
-// do nothing but the dependent memory traffic of that critical path, so that
+// token's index words, then the ring rows they name).  These kernels take a
+// decode kernel's launch shape (n warps, a chosen number per CTA) and do
+// nothing but the dependent memory traffic of that critical path, so that
 // timing them with the same method as the decode call gives its floor:
 //   hops 0  wait for the predecessor grid (programmatic dependent launch) and
 //           return: the launch-and-completion cost alone;

@@ -446,8 +446,8 @@ ckv_status ckv_c128_online_prefill_counted_fp8(float* state, int64_t num_slots, 
 /*
  * Latency floor of a decode-sized launch: a measurement aid with no
  * counterpart in the sources.  Launches n_warps warps, warps_per_cta to a CTA
- * (the pooled decode update's launch shape is one warp per request, 4 to a
- * CTA), each of which first waits for the preceding grid when use_pdl is set
+ * (the pooled decode update's launch shape is one CTA of two warps per
+ * request), each of which first waits for the preceding grid when use_pdl is set
  * (programmatic dependent launch), then does only dependent memory traffic:
  *   hops == 0  nothing (the cost of launching and completing the grid);
  *   hops == 1  loads idx[w] and stores it to the first 4 bytes of row w of out
