@@ -386,6 +386,37 @@ def test_kpool_decode_long_sequences_and_across_calls(ck, ora, P):
     check_rows(ora, gx, gxb, gyb, gq, gs, ref, True, f"across calls P={P}")
 
 
+def test_kpool_decode_strided_key_score(ck, ora):
+    """Key and score rows as views of one fused per-token buffer (batch stride
+    N * 3 * 128 + 64, token stride 3 * 128 elements): the C ABI takes both
+    strides; the result equals the oracle's on contiguous copies."""
+    from compressed_kv_attention_gated_gb300 import synth
+
+    d = synth.pooled_decode("cpu", seed=21, B=96, N=5)
+    B, N = d["B"], d["N"]
+    buf = torch.randn((B, N * 3 * D + 64), dtype=torch.float32).to(torch.bfloat16)
+    fused = buf[:, :N * 3 * D].view(B, N, 3, D)
+    fused[:, :, 1] = d["key"]
+    fused[:, :, 2] = d["score"]
+    gbuf = buf.cuda()
+    gf = gbuf[:, :N * 3 * D].view(B, N, 3, D)
+    gk, gsc = gf[:, :, 1], gf[:, :, 2]
+    assert gk.stride() == (N * 3 * D + 64, 3 * D, 1) and not gk.is_contiguous()
+    dev = "cuda"
+    cache, ring = d["kv_cache"].to(dev), d["ring"].to(dev)
+    tx = torch.full((B * N, D), float("nan"), device=dev)
+    txb = torch.zeros((B * N, D), dtype=torch.bfloat16, device=dev)
+    tyb = torch.zeros((B * N, D), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros((1,), dtype=torch.int32, device=dev)
+    ck.ckv_kpool_decode_update(cache, ring, d["tail_slot_mapping"].to(dev), d["slot_mapping"].to(dev),
+                               d["positions"].to(dev), gk, gsc, d["ape"].to(dev), tap_x=tx, tap_xb=txb, tap_yb=tyb,
+                               use_pdl=True, err_word=err)
+    torch.cuda.synchronize()
+    oref = _oracle_decode(ora, d, True)
+    n, _ = _compare_decode(ora, d, (cache, ring, tx, txb, tyb, int(err.item())), oref, True, "strided key/score")
+    assert n > 10
+
+
 def test_kpool_decode_golden_gating_and_block_clamp(ck):
     """The hand-derived pooled-decode fixture (closing token with a negative
     tail slot reads ring block 0 and stashes nothing; closing slot without a
