@@ -455,6 +455,34 @@ def test_kpool_decode_bad_block_flags(ck):
     assert np.all(r[0, 0, 4] == 0x3F80) and np.all(r[0, 0, 3] == 0)
 
 
+def test_kpool_decode_bad_cache_location_flags_and_stashes(ck):
+    """A closing token whose cache location is past the cache: the cache-location
+    bit is set, no cache byte changes, the token is still stashed, and the
+    other request of the call closes its pool normally."""
+    P = 16
+    B, N = 2, 1
+    ring = torch.zeros((2, 2, P, D), dtype=torch.bfloat16, device="cuda")
+    ps = 16
+    cache = torch.full((1, ps, D + 4), 0x37, dtype=torch.uint8, device="cuda")
+    tsm = torch.tensor([[0 * P + 15], [1 * P + 15]], dtype=torch.int32, device="cuda")
+    sm = torch.tensor([[ps], [3]], dtype=torch.int32, device="cuda")  # request 0: one past the end
+    pos = torch.tensor([[15], [31]], dtype=torch.int32, device="cuda")
+    key = torch.full((B, N, D), 2.0, dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    ck.ckv_kpool_decode_update(cache, ring, tsm, sm, pos, key, key, torch.zeros((P, D), device="cuda"), err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0x4
+    c = u8(cache).reshape(-1)
+    row3 = c[3 * D:4 * D]
+    assert not np.all(row3 == 0x37), "request 1's pool was not written"
+    c2 = c.copy()
+    c2[3 * D:4 * D] = 0x37
+    c2[ps * D + 12:ps * D + 16] = 0x37
+    assert np.all(c2 == 0x37), "bytes other than request 1's row and scale changed"
+    r = bf16_bits(ring)
+    assert np.all(r[0, 0, 15] == 0x4000) and np.all(r[0, 1, 15] == 0x4000), "request 0's token was not stashed"
+
+
 def _seed_case(P, lens, seed):
     g = torch.Generator().manual_seed(seed)
     blocks = torch.randperm(len(lens), generator=g)
