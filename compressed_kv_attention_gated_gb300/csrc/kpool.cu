@@ -599,9 +599,11 @@ cudaError_t compress_bulk(const KpoolCompressArgs& a, bool use_pdl, cudaStream_t
 
 // Pool -> token index expansion with the tail appended: one warp per row.  The
 // warp copies the row's pool ids into shared memory with one coalesced pass,
-// then writes the row's columns 32 at a time (coalesced int32 stores) with no
-// global load inside the loop; column -> (pool, offset) uses a shift and a
-// mask when P is a power of two, a 32-bit division otherwise.
+// then writes the row's columns four at a time per lane as 16-byte stores (a
+// row starts on a 4-byte boundary only, so the columns before its first
+// 16-byte boundary and the last ones are written one by one), with no global
+// load inside the loop; column -> (pool, offset) uses a shift and a mask when
+// P is a power of two, a 32-bit division otherwise.
 constexpr int kExpandWarps = 8;
 constexpr int kExpandMaxGroups = 2048;  // pool ids per row staged in smem (8 KB per warp)
 
@@ -625,18 +627,27 @@ __global__ void __launch_bounds__(kExpandWarps * 32)
     const int64_t tail_count = s - tail_start;
     __syncwarp();
     int32_t* dst = a.out + r * cols;
-    for (uint32_t c = lane; c < cols; c += 32) {
-      int32_t v;
+    auto value = [&](uint32_t c) -> int32_t {
       if (c < gcols) {
         const uint32_t g = pow2 ? (c >> shift) : c / P;
         const int64_t id = ids[g];
-        v = id >= 0 ? static_cast<int32_t>(id * P + (c - g * P)) : -1;
-      } else {
-        const int64_t i = c - gcols;
-        v = i < tail_count ? static_cast<int32_t>(tail_start + i) : -1;
+        return id >= 0 ? static_cast<int32_t>(id * P + (c - g * P)) : -1;
       }
-      dst[c] = v;
+      const int64_t i = c - gcols;
+      return i < tail_count ? static_cast<int32_t>(tail_start + i) : -1;
+    };
+    // columns [0, head) up to the row's first 16-byte boundary, then four per
+    // lane per step, then the last (cols - head) % 4
+    const uint32_t head = min(cols, ((16u - (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(dst)) & 15u)) & 15u) / 4u);
+    if (lane < head) dst[lane] = value(lane);
+    const uint32_t nvec = (cols - head) / 4;
+    int4* vdst = reinterpret_cast<int4*>(dst + head);
+    for (uint32_t v = lane; v < nvec; v += 32) {
+      const uint32_t c = head + 4 * v;
+      vdst[v] = make_int4(value(c), value(c + 1), value(c + 2), value(c + 3));
     }
+    const uint32_t done = head + 4 * nvec;
+    if (done + lane < cols) dst[done + lane] = value(done + lane);
     __syncwarp();
   }
 }
