@@ -5,12 +5,13 @@
 // _kpool_tail_seed_kernel).  Those are AMD Triton kernels with one program per
 // request/pool and a 128-wide block; the design here is our own for sm_103a:
 //
-//   * one warp per pool (or per request), lane l owning channels 4l..4l+3, so
-//     every key/score slot row (256 B of bf16) is one coalesced 8-byte-per-lane
-//     load and every FP8 output row (128 B) one 4-byte-per-lane store;
-//   * all P slot rows of a pool are loaded before any arithmetic (P * 16 B in
-//     flight per lane), the per-slot bias table is staged in shared memory once
-//     per CTA;
+//   * one-shot: one warp per pool, lane l owning channels 4l..4l+3, so every
+//     key/score slot row (256 B of bf16) is one coalesced 8-byte-per-lane load
+//     and every FP8 output row (128 B) one 4-byte-per-lane store; all P slot
+//     rows of a pool are loaded before any arithmetic (P * 16 B in flight per
+//     lane), the per-slot bias table is staged in shared memory once per CTA;
+//   * decode: one CTA of two warps per request, thread t owning the channel
+//     pair (2t, 2t + 1) (described at the kernel);
 //   * exact two-pass softmax from registers: z = score + ape for the P slots,
 //     max, then one ex2 per element;
 //   * for large batches, a persistent variant in which every warp streams its
