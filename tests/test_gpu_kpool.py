@@ -386,6 +386,66 @@ def test_kpool_decode_long_sequences_and_across_calls(ck, ora, P):
     check_rows(ora, gx, gxb, gyb, gq, gs, ref, True, f"across calls P={P}")
 
 
+@pytest.mark.parametrize("P", [1, 2, 4, 8, 16])
+def test_kpool_decode_random_calls(ck, ora, P):
+    """Random small calls in sequence on one ring and cache: random request
+    counts and token counts per call (several pool closings per request and
+    per group of four tokens when P is small), random padding anywhere, random
+    tail blocks, positions that continue across calls, both FP8 scales.  Ring
+    bit-exact after every call; every closing row checked stage by stage."""
+    rng = np.random.default_rng(1000 + P)
+    B, blocks, ps = 9, 12, 8
+    ring0 = torch.from_numpy(rng.standard_normal((blocks, 2, P, D)).astype(np.float32)).to(torch.bfloat16)
+    ring_g = ring0.cuda()
+    rring = bf16_bits(ring0).copy()
+    cap = 64
+    cache0 = torch.full(((B * cap + ps - 1) // ps, ps, D + 4), 0x29, dtype=torch.uint8)
+    cache_g = cache0.cuda()
+    rcache = u8(cache0).copy()
+    ape = torch.from_numpy((rng.standard_normal((P, D)) * 0.1).astype(np.float32))
+    block_of = rng.permutation(blocks)[:B]
+    next_pos = rng.integers(0, 3 * P, B)
+    for call in range(6):
+        N = int(rng.integers(1, 3 * P + 3))
+        pos = next_pos[:, None] + np.arange(N)[None, :]
+        next_pos = next_pos + N
+        pad = rng.random((B, N)) < 0.15
+        ts = block_of[:, None] * P + pos % P
+        sm = np.where(pos % P == P - 1, np.arange(B)[:, None] * cap + (pos // P) % cap, -1)
+        ts_pad, sm_pad, pos_pad = (np.where(pad, -1, x).astype(np.int32) for x in (ts, sm, pos))
+        # a few padded-slot cases: a token keeps its position but has no cache location
+        nosm = (rng.random((B, N)) < 0.05) & ~pad
+        sm_pad = np.where(nosm, -1, sm_pad).astype(np.int32)
+        key = torch.from_numpy(rng.standard_normal((B, N, D)).astype(np.float32)).to(torch.bfloat16)
+        score = torch.from_numpy((rng.standard_normal((B, N, D)) * 2).astype(np.float32)).to(torch.bfloat16)
+        round_scale = bool(call % 2)
+        n_tok = B * N
+        tx = torch.full((n_tok, D), float("nan"), device="cuda")
+        txb = torch.zeros((n_tok, D), dtype=torch.bfloat16, device="cuda")
+        tyb = torch.zeros((n_tok, D), dtype=torch.bfloat16, device="cuda")
+        err = torch.zeros((1,), dtype=torch.int32, device="cuda")
+        t = lambda x: torch.from_numpy(x).cuda()
+        ck.ckv_kpool_decode_update(cache_g, ring_g, t(ts_pad), t(sm_pad), t(pos_pad), key.cuda(), score.cuda(),
+                                   ape.cuda(), round_scale=round_scale, tap_x=tx, tap_xb=txb, tap_yb=tyb,
+                                   use_pdl=bool(call % 3 == 0), err_word=err)
+        r = ora.kpool_decode_update(rcache, ps, rring, ts_pad, sm_pad, pos_pad, bf16_bits(key), bf16_bits(score),
+                                    f32(ape), round_scale=round_scale, taps=True)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        np.testing.assert_array_equal(bf16_bits(ring_g), rring, err_msg=f"ring after call {call}")
+        fsm, fpos = sm_pad.reshape(-1), pos_pad.reshape(-1)
+        closing = np.nonzero((fsm >= 0) & (fpos >= 0) & (fpos % P == P - 1))[0]
+        if len(closing) == 0:
+            continue
+        gq, gs = cache_rows(u8(cache_g), ps, D, fsm[closing])
+        rq, rs = cache_rows(rcache, ps, D, fsm[closing])
+        sub = {k: v[closing] for k, v in r.items()}
+        sub["q"], sub["scale"] = rq, rs
+        check_rows(ora, f32(tx)[closing], bf16_bits(txb)[closing], bf16_bits(tyb)[closing], gq, gs, sub,
+                   round_scale, f"random calls P={P} call={call}")
+        assert np.all(np.isnan(f32(tx)[np.setdiff1d(np.arange(n_tok), closing)])), "taps of non-closing tokens"
+
+
 def test_kpool_decode_strided_key_score(ck, ora):
     """Key and score rows as views of one fused per-token buffer (batch stride
     N * 3 * 128 + 64, token stride 3 * 128 elements): the C ABI takes both
