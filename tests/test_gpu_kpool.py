@@ -713,3 +713,26 @@ def test_expand_pools_and_append_tail_vs_oracle(ck, ora, P):
         torch.cuda.synchronize()
         ref = ora.expand_pools_and_append_tail(ids.numpy(), seq.numpy(), P)
         np.testing.assert_array_equal(out.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+@pytest.mark.parametrize("P", [1, 4, 16])
+def test_expand_output_off_16_byte_boundary(ck, ora, P, offset):
+    """The output starts 4, 8 or 12 bytes past a 16-byte boundary: every row's
+    columns before its first 16-byte boundary and after its last one are
+    written one by one, the rest four at a time; the element before the output
+    and the one after it keep their canary."""
+    g = torch.Generator().manual_seed(P * 10 + offset)
+    for rows, groups in ((5, 3), (1000, 7), (33, 64)):
+        ids = torch.randint(-1, 900, (rows, groups), generator=g, dtype=torch.int32)
+        seq = torch.randint(0, 20000, (rows,), generator=g, dtype=torch.int64)
+        cols = groups * P + P - 1
+        big = torch.full((rows * cols + 8,), -7, dtype=torch.int32, device="cuda")
+        out = big[offset:offset + rows * cols].view(rows, cols)
+        assert out.data_ptr() % 16 == 4 * offset
+        ck.ckv_expand_pools_and_append_tail(ids.cuda(), seq.cuda(), P, out=out)
+        torch.cuda.synchronize()
+        ref = ora.expand_pools_and_append_tail(ids.numpy(), seq.numpy(), P)
+        np.testing.assert_array_equal(out.cpu().numpy(), ref)
+        b = big.cpu().numpy()
+        assert np.all(b[:offset] == -7) and np.all(b[offset + rows * cols:] == -7)
