@@ -762,7 +762,9 @@ def rotation_timings(case, replays=100, warmup=20, round_scale=True, instances=N
     its running max moves at the workload's own rate instead of never (a
     replay into states it already updated leaves every max unchanged).  The
     bytes it physically writes (the max-row sectors it leaves alone excluded)
-    are reported beside the algorithmic bytes.
+    are reported beside the algorithmic bytes.  c128_decode_fp8: the same
+    with the FP8 output stage instead of the fp32 rows, each instance writing
+    its own cache rows.
 
     Pooled decode: the instances share one cache tensor, each writing its own
     rows (location r * B + b for request b of instance r); round_scale picks
@@ -790,19 +792,35 @@ def rotation_timings(case, replays=100, warmup=20, round_scale=True, instances=N
     flush = torch.empty((2 * l2,), dtype=torch.uint8, device=dev)
     restore = None
     extra = {}
-    if case == "c128_decode":
+    if case in ("c128_decode", "c128_decode_fp8"):
         first = synth.c128_decode(dev, seed=100)
-        nbytes = c128_decode_bytes(first)[0]
+        nbytes, closing = c128_decode_bytes(first)
+        fp8 = case == "c128_decode_fp8"
+        B, D = first["B"], first["D"]
+        if fp8:
+            # no fp32 output rows; per closing request its cache location and
+            # FP8 row (D code bytes + one fp32 scale per 128 channels)
+            nbytes += closing * (8 + D + 4 * (D // 128) - 4 * D)
         R = max(kMinInstances, math.ceil(4 * l2 / nbytes))
+        if fp8:
+            ps = 64
+            cache = torch.zeros(((R * B + ps - 1) // ps, ps, D + 4 * (D // 128)), device=dev, dtype=torch.uint8)
 
         def make(r):
             d = first if r == 0 else synth.c128_decode(dev, seed=100 + r)
             d["state0"] = d["state"].clone()
+            if fp8:
+                d["cache_loc"] = torch.arange(r * B, (r + 1) * B, device=dev, dtype=torch.int64)
             return d
 
         def call(d, pdl):
-            ck.ckv_c128_online_decode(d["state"], d["input"], d["out"], d["ape"], d["indices"], d["seq_lens"],
-                                      use_pdl=pdl, err_word=err)
+            if fp8:
+                ck.ckv_c128_online_decode_fp8(d["state"], d["input"], None, d["ape"], d["indices"], d["seq_lens"],
+                                              cache, d["cache_loc"], round_scale=round_scale, use_pdl=pdl,
+                                              err_word=err)
+            else:
+                ck.ckv_c128_online_decode(d["state"], d["input"], d["out"], d["ape"], d["indices"], d["seq_lens"],
+                                          use_pdl=pdl, err_word=err)
 
         def restore(inst):
             for d in inst:
@@ -849,7 +867,7 @@ def rotation_timings(case, replays=100, warmup=20, round_scale=True, instances=N
 
         nbytes = {0: 0, 1: n * 8, 2: n * 516, 3: n * (48 + 1024 + 4)}[hops]
     else:
-        raise SystemExit("--rotate applies to --case c128_decode, kpool_decode or latency_floor0|1|2")
+        raise SystemExit("--rotate applies to --case c128_decode, c128_decode_fp8, kpool_decode or latency_floor<h>")
     if instances:
         R = int(instances)
     inst = [make(r) for r in range(R)]
@@ -858,7 +876,7 @@ def rotation_timings(case, replays=100, warmup=20, round_scale=True, instances=N
     stream = torch.cuda.Stream(dev)
     res = {"case": case, "mode": "rotate", "instances": R, "l2_bytes": l2, "bytes_per_call": nbytes,
            "replays": replays, "l2_flush_before_each_replay": flush_each}
-    if case == "kpool_decode":
+    if case in ("kpool_decode", "c128_decode_fp8"):
         res["round_scale"] = bool(round_scale)
 
     def before(warm):
@@ -885,7 +903,7 @@ def rotation_timings(case, replays=100, warmup=20, round_scale=True, instances=N
                 t.append(e0.elapsed_time(e1) * 1e3 / n_calls)
         return float(np.median(t))
 
-    if case == "c128_decode":
+    if case in ("c128_decode", "c128_decode_fp8"):
         # bytes the call physically writes: the max-row sectors (8 channels, 32
         # bytes) of open requests whose new maxima equal the stored ones are left
         # alone by the kernel

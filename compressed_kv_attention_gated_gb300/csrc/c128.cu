@@ -21,9 +21,12 @@
 //              passes are two launches in stream order (optionally chained
 //              by programmatic dependent launch).
 //   FP8 stage (the _fp8 calls; kFp8 instantiations) -- each emitted row is
-//              staged in shared memory and stored, 128-channel block by
-//              block, through the pooled path's rotation and quantisation
-//              (ckv_fp8.cuh) into a paged FP8 cache.
+//              stored, 128-channel block by block, through the pooled path's
+//              rotation and quantisation (ckv_fp8.cuh) into a paged FP8
+//              cache.  The decode at D >= 256 rotates straight from the
+//              closing request's registers (its threads already hold each
+//              block in the rotation's lane layout); the decode at D = 128
+//              and the prefill stage the row in shared memory first.
 #include <type_traits>
 
 #include "ckv_device.cuh"
@@ -55,6 +58,9 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinBlocks)
   constexpr int kTpr = D / (4 * G);             // threads per request (even)
   constexpr int kRpc = kDecodeThreads / kTpr;   // requests per CTA
   constexpr int kSpan = D / G;                  // channel distance between groups
+  // FP8 stage straight from registers when a request is whole warps and each
+  // group spans whole 128-channel blocks (D >= 256 with two groups)
+  constexpr bool kWarpRows = kTpr % 32 == 0 && kSpan % 128 == 0;
   pdl_wait();
   pdl_trigger();
   const int t = threadIdx.x % kTpr;
@@ -69,7 +75,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinBlocks)
   // its latency is not paid at the stage's barrier
   int64_t cache_loc = kNoRow;
   if constexpr (kFp8) {
-    if (in_batch && t == 0) cache_loc = a.cache_loc[b];
+    if (in_batch && (kWarpRows || t == 0)) cache_loc = a.cache_loc[b];
   }
   const int col = 4 * t;
   const InT* in = static_cast<const InT*>(a.input) + static_cast<int64_t>(in_batch ? b : 0) * 2 * D;
@@ -149,7 +155,20 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinBlocks)
       }
     }
   }
-  if constexpr (kFp8) {
+  if constexpr (kFp8 && kWarpRows) {
+    // the request's warps hold whole blocks in the rotation's lane layout:
+    // channels 4l..4l+3 of block t / 32 + (D / 256) g in lane l's group g
+    if (ok && p == 127) {  // the same for every thread of the request
+      if (cache_loc < 0 || cache_loc >= a.num_pages * a.page_size) {
+        if (t == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
+      } else {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          fp8_block_store(nkv[g], a.cache, a.page_size, cache_loc, kBlocks, t / 32 + (kSpan / 128) * g, t & 31,
+                          a.round_scale != 0);
+      }
+    }
+  } else if constexpr (kFp8) {
     // closing rows staged per CTA, then one warp per 128-channel block
     __shared__ __align__(16) float s_row[kRpc][D];
     __shared__ int64_t s_loc[kRpc];

@@ -103,17 +103,24 @@ __device__ __forceinline__ void cache_write_block(uint8_t* cache, int64_t page_s
   if (lane == 0) reinterpret_cast<float*>(base + page_size * row_bytes)[tok * blocks + j] = scale;
 }
 
-// One warp stores block j of a staged fp32 row into the paged FP8 cache
-// (bf16 -> Hadamard-128 -> bf16 -> absmax FP8, one scale per block).
-__device__ __forceinline__ void fp8_block_store(const float* row128, uint8_t* cache, int64_t page_size,
-                                                int64_t loc, int blocks, int j, int lane, bool round_scale) {
-  const float4 v = *reinterpret_cast<const float4*>(row128 + 4 * lane);
+// One warp stores block j of an fp32 row into the paged FP8 cache (bf16 ->
+// Hadamard-128 -> bf16 -> absmax FP8, one scale per block); lane l passes
+// channels 4l..4l+3 of the block.
+__device__ __forceinline__ void fp8_block_store(float4 v, uint8_t* cache, int64_t page_size, int64_t loc,
+                                                int blocks, int j, int lane, bool round_scale) {
   const float x[4] = {v.x, v.y, v.z, v.w};
   float xb[4], yb[4], scale;
   uint32_t codes;
   if (round_scale) rotate_quantize<true>(x, lane, codes, scale, xb, yb);
   else rotate_quantize<false>(x, lane, codes, scale, xb, yb);
   cache_write_block(cache, page_size, loc, blocks, j, lane, codes, scale);
+}
+
+// The same for a row staged in memory (128 channels from row128).
+__device__ __forceinline__ void fp8_block_store(const float* row128, uint8_t* cache, int64_t page_size,
+                                                int64_t loc, int blocks, int j, int lane, bool round_scale) {
+  fp8_block_store(*reinterpret_cast<const float4*>(row128 + 4 * lane), cache, page_size, loc, blocks, j, lane,
+                  round_scale);
 }
 
 }  // namespace ckv

@@ -212,10 +212,13 @@ def test_prefill_fp8_long_context_full(ck, ora):
                          "c128 prefill fp8 long context 8x131072")
 
 
-def test_fp8_bad_location_flagged_and_skipped(ck, ora):
+@pytest.mark.parametrize("D", [128, 256, 512])
+def test_fp8_bad_location_flagged_and_skipped(ck, ora, D):
+    """D = 128 stages the closing rows per CTA; D = 256 and 512 quantise from
+    the request's registers: both skip and flag an out-of-range location."""
     from compressed_kv_attention_gated_gb300 import synth
 
-    B, D = 64, 256
+    B = 64
     d = synth.c128_decode("cpu", seed=5, B=B, D=D, num_slots=128)
     d["seq_lens"] = torch.full((B,), 128, dtype=torch.int32)  # every request closes
     cache0, ps = _cache(B, D)
