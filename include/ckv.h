@@ -467,8 +467,8 @@ ckv_status ckv_c128_online_prefill_counted_fp8(float* state, int64_t num_slots, 
  *              [0, num_rows) makes that warp skip its row (hops == 2)
  *   rows       device [num_rows][256 bytes], 8-byte aligned (hops >= 2)
  *   out        device [n_warps][256 bytes], 8-byte aligned (hops >= 1)
- * Sizes outside hops 0..3, n_warps >= 1, 1 <= warps_per_cta <= 32 (and the
- * hops == 3 minimums) return CKV_ERR_SHAPE and launch nothing.
+ * Sizes outside hops 0..3, 1 <= n_warps <= 2^30, 1 <= warps_per_cta <= 32
+ * (and the hops == 3 minimums) return CKV_ERR_SHAPE and launch nothing.
  */
 ckv_status ckv_latency_probe(int32_t hops, const int32_t* idx, const void* rows, int64_t num_rows, void* out,
                              int32_t n_warps, int32_t warps_per_cta, int32_t use_pdl, void* stream);

@@ -61,6 +61,7 @@ def test_validation_rejects_before_launch(lib):
     assert lib.ckv_latency_probe(3, one, one, 8, one, 64, 4, 0, None) == 2    # ... and >= 9 rows
     assert lib.ckv_latency_probe(3, one, None, 4096, one, 64, 4, 0, None) == 1
     assert lib.ckv_latency_probe(2, one, one, 4, one, 0, 4, 0, None) == 2
+    assert lib.ckv_latency_probe(0, one, one, 4, one, (1 << 30) + 1, 4, 0, None) == 2  # grid size
     assert lib.ckv_latency_probe(1, one, one, 4, one, 8, 33, 0, None) == 2
     assert lib.ckv_latency_probe(2, one, None, 4, one, 8, 4, 0, None) == 1
     assert lib.ckv_latency_probe(1, None, None, 0, one, 8, 4, 0, None) == 1
