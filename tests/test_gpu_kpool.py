@@ -715,6 +715,22 @@ def test_expand_pools_and_append_tail_vs_oracle(ck, ora, P):
         np.testing.assert_array_equal(out.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("P", [3, 5, 12, 1000, 1024])
+def test_expand_any_pool_size_and_most_groups(ck, ora, P):
+    """Pool sizes that are not a power of two take the kernel's division path
+    (column -> pool by a 32-bit division); rows of 2048 pool ids (the most a
+    call accepts) with P up to 1024 are the widest rows.  Bit-exact against
+    the oracle."""
+    g = torch.Generator().manual_seed(1000 + P)
+    for rows, groups in ((7, 5), (3, 2048)):
+        ids = torch.randint(-1, 2000, (rows, groups), generator=g, dtype=torch.int32)
+        seq = torch.randint(0, groups * P + P, (rows,), generator=g, dtype=torch.int64)
+        out = ck.ckv_expand_pools_and_append_tail(ids.cuda(), seq.cuda(), P)
+        torch.cuda.synchronize()
+        ref = ora.expand_pools_and_append_tail(ids.numpy(), seq.numpy(), P)
+        np.testing.assert_array_equal(out.cpu().numpy(), ref)
+
+
 @pytest.mark.parametrize("offset", [1, 2, 3])
 @pytest.mark.parametrize("P", [1, 4, 16])
 def test_expand_output_off_16_byte_boundary(ck, ora, P, offset):
