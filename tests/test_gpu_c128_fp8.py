@@ -149,7 +149,7 @@ def _prefill(ck, d, cp, wp, nc, nw, out, cache, cache_loc, round_scale, use_pdl,
 @pytest.mark.parametrize("use_pdl", [False, True])
 @pytest.mark.parametrize("round_scale", [True, False])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("D", [128, 512])
+@pytest.mark.parametrize("D", [128, 256, 512])
 def test_prefill_fp8(variant, ck, ora, D, dtype, round_scale, use_pdl):
     from compressed_kv_attention_gated_gb300 import synth
 
