@@ -34,6 +34,9 @@ MUTANTS = [
     ("power-of-two and linear scales swapped",
      "const float scale = round_scale ? pow2_ceil(v) : v;",
      "const float scale = round_scale ? v : pow2_ceil(v);"),
+    ("linear scale: multiply by the reciprocal instead of dividing",
+     "float t = bf16_to_float(yb[d]) / scale;",
+     "float t = bf16_to_float(yb[d]) * (1.0f / scale);"),
     ("absmax floor 1e-3 instead of 1e-4",
      "absmax = std::max(absmax, 1e-4f);",
      "absmax = std::max(absmax, 1e-3f);"),

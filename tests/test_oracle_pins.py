@@ -197,6 +197,58 @@ def test_quantize_scale_invariants(ora):
             assert np.all(np.abs(dec - t) <= quantum / 2 * (1 + 1e-6))
 
 
+def _fp32_nearest(q):
+    """The fp32 value nearest to the positive rational q (ties to even), exactly."""
+    from fractions import Fraction
+
+    e = q.numerator.bit_length() - q.denominator.bit_length()
+    if Fraction(2) ** e > q:
+        e -= 1
+    assert -126 <= e < 128  # normal range
+    ulp = Fraction(2) ** (e - 23)
+    n, r = divmod(q, ulp)
+    if r * 2 > ulp or (r * 2 == ulp and n % 2 == 1):
+        n += 1
+    return n * ulp
+
+
+def _e4m3_nearest_code(t):
+    """The e4m3 code nearest to the non-negative rational t < 2^-6 (the
+    subnormal range, quantum 2^-9; ties to even)."""
+    from fractions import Fraction
+
+    q = Fraction(1, 512)
+    n, r = divmod(t, q)
+    if r * 2 > q or (r * 2 == q and n % 2 == 1):
+        n += 1
+    return int(n)  # subnormal codes are the multiple itself (8 = the smallest normal, code 0x08)
+
+
+@pytest.mark.parametrize("am_bits,y_bits", [(0x3F84, 0x3784), (0x3F98, 0x3798), (0x3FA3, 0x37A3)])
+def test_quantize_linear_scale_divides(ora, am_bits, y_bits):
+    """Reading 4: q = y / scale is one IEEE fp32 division.  The row holds its
+    absmax a and one element y = a * 2^-16, so y / scale lies within an fp32
+    ulp of the e4m3 midpoint 3.5 * 2^-9: fp32(y / scale) and fp32(y *
+    fp32(1 / scale)) round to different codes.  The expected code and scale
+    are computed here with exact rational arithmetic."""
+    from fractions import Fraction
+
+    def bf16(bits):
+        return Fraction(float(np.array([bits << 16], np.uint32).view(np.float32)[0]))
+
+    a, y = bf16(am_bits), bf16(y_bits)
+    inv448 = _fp32_nearest(Fraction(1, 448))
+    scale = _fp32_nearest(a * inv448)
+    want = _e4m3_nearest_code(_fp32_nearest(y / scale))
+    other = _e4m3_nearest_code(_fp32_nearest(y * _fp32_nearest(1 / scale)))
+    assert want != other  # the case tells the two apart
+    row = np.zeros(128, np.uint16)
+    row[0], row[1] = am_bits, y_bits
+    q, sc = ora.quantize_rows(row, False)
+    assert Fraction(float(sc)) == scale
+    assert int(q[1]) == want and int(q[0]) == 0x7E  # the absmax itself maps to 448
+
+
 def test_quantize_floor_on_zero_row(ora):
     q, sc = ora.quantize_rows(np.zeros(128, np.uint16), True)
     assert sc == ora.pow2_ceil(np.float32(1e-4) * np.float32(1.0 / 448.0))
