@@ -481,7 +481,8 @@ def test_kpool_decode_golden_gating_and_block_clamp(ck):
     """The hand-derived pooled-decode fixture (closing token with a negative
     tail slot reads ring block 0 and stashes nothing; closing slot without a
     cache location only stashes; open slot with a negative tail slot does
-    nothing) through the C ABI."""
+    nothing; a stash lands in its position's slot of its tail slot's block)
+    through the C ABI."""
     from test_oracle_pins import _KD_GOLDEN as fx, kpool_decode_golden_check, kpool_decode_golden_inputs
 
     a = kpool_decode_golden_inputs(fx)

@@ -73,6 +73,15 @@ MUTANTS = [
     ("pool expansion treats pool id 0 as invalid",
      "o[g * P + k] = id >= 0 ? static_cast<int32_t>(id * P + k) : -1;",
      "o[g * P + k] = id > 0 ? static_cast<int32_t>(id * P + k) : -1;"),
+    ("Hadamard fp32 butterflies in descending span order",
+     "  for (int h = 1; h < 128; h <<= 1) {\n    for (int i = 0; i < 128; ++i) {\n      if (i & h) continue;",
+     "  for (int h = 64; h >= 1; h >>= 1) {\n    for (int i = 0; i < 128; ++i) {\n      if (i & h) continue;"),
+    ("prefill emits a row at chunk position 126",
+     "if (last % 128 == 127) {",
+     "if (last % 128 >= 126) {"),
+    ("pooled decode stashes at the tail slot's own offset",
+     "std::memcpy(kring + slot * D, kcur, D * 2);",
+     "std::memcpy(kring + (std::max(tslot, 0) % P) * D, kcur, D * 2);"),
     ("c128 FP8 store: block scales laid out block-major",
      "std::memcpy(base + page_size * D + 4 * (tok * blocks + j), &scale, 4);",
      "std::memcpy(base + page_size * D + 4 * (j * page_size + tok), &scale, 4);"),

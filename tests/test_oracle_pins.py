@@ -174,6 +174,27 @@ def test_hadamard_fp32_butterfly_vs_exact(ora):
         assert np.max(np.abs(back - x)) <= 2e-6 * max(1.0, np.max(np.abs(x)))
 
 
+def test_hadamard_fp32_rounding_path_worked_example(ora):
+    """The fp32 rotation's rounding path (butterfly spans 1, 2, ..., 64 in
+    ascending order, each (u + v, u - v) rounded to fp32 to nearest even, then
+    one multiply by fp32(1/sqrt(128))), worked by hand on x = (1, 2^-24,
+    2^-23, 0, ..., 0):
+      span 1: 1 + 2^-24 is a tie between 1 and 1 + 2^-23 -> 1 (even);
+              1 - 2^-24 exact; 2^-23 + 0 = 2^-23 - 0 = 2^-23;
+      span 2: 1 + 2^-23 and 1 - 2^-23 exact; (1 - 2^-24) + 2^-23 = 1 + 2^-24,
+              a tie -> 1; (1 - 2^-24) - 2^-23 = 1 - 3 * 2^-24 exact;
+      spans 4..64 pair every value with a zero: output i is the value at i % 4.
+    Spans in the other order would round the first output to 1 + 2^-22 instead
+    (span 2 first gives 1 + 2^-23 and 2^-24, whose sum is a tie -> 1 + 2^-22),
+    and the exact transform gives (1 + 3 * 2^-24) / sqrt(128)."""
+    x = np.zeros(128, np.float32)
+    x[0], x[1], x[2] = 1.0, 2.0 ** -24, 2.0 ** -23
+    before_scale = np.array([1 + 2.0 ** -23, 1.0, 1 - 2.0 ** -23, 1 - 3 * 2.0 ** -24], np.float32)
+    c = np.float32(1.0 / math.sqrt(128.0))
+    want = np.tile(before_scale * c, 32)  # one fp32 multiply per value
+    np.testing.assert_array_equal(ora.hadamard128_fp32(x), want)
+
+
 # ------------------------------------------------------------------- quantise
 def test_quantize_scale_invariants(ora):
     rng = np.random.default_rng(7)
@@ -500,7 +521,7 @@ _KD_GOLDEN = json.load(open(os.path.join(GOLDEN, "kpool_decode_examples.json")))
 def kpool_decode_golden_inputs(fx, D=128):
     """Arrays of the pooled-decode fixture: one token per request."""
     P = fx["P"]
-    ring = np.zeros((2, 2, P, D), np.float32)
+    ring = np.zeros((len(fx["ring"]["key"]), 2, P, D), np.float32)
     ring[:, 0] = np.array(fx["ring"]["key"], np.float32)[:, :, None]
     ring[:, 1] = np.array(fx["ring"]["score"], np.float32)[:, :, None]
     toks = fx["tokens"]
@@ -529,7 +550,7 @@ def kpool_decode_golden_check(fx, cache, ring, D=128):
     rest[row0:row0 + D] = False
     rest[sc0:sc0 + 4] = False
     assert np.all(flat[rest] == fx["canary"]), "only the closing row's bytes change"
-    want = np.zeros((2, 2, P, D), np.float32)
+    want = np.zeros((len(e["ring_key"]), 2, P, D), np.float32)
     want[:, 0] = np.array(e["ring_key"], np.float32)[:, :, None]
     want[:, 1] = np.array(e["ring_score"], np.float32)[:, :, None]
     np.testing.assert_array_equal(ring, _bf16_bits(want))
@@ -539,7 +560,8 @@ def test_kpool_decode_golden_gating_and_block_clamp(ora):
     """Hand-derived: a closing token whose tail slot is negative still closes
     its pool, from ring block 0 (block = max(tail_slot, 0) // P), and stashes
     nothing; a token at the closing slot without a cache location only stashes;
-    an open slot with a negative tail slot changes nothing."""
+    an open slot with a negative tail slot changes nothing; a token is stashed
+    in its position's slot of its tail slot's block."""
     fx = _KD_GOLDEN
     a = kpool_decode_golden_inputs(fx)
     ring, cache = a["ring"].copy(), a["cache"].copy()
@@ -823,6 +845,32 @@ def test_c128_prefill_split_equals_whole(ora):
         if sw[0]:
             st = fs.astype(np.float32)
     np.testing.assert_allclose(st[0], whole_fs[0], rtol=1e-5, atol=1e-5)
+
+
+def test_c128_prefill_emits_exactly_at_chunk_position_127(ora):
+    # c128 page, flash_c128_online_prefill: a chunk closes at its 128th token
+    # (chunk position 127), which emits the row; a request whose last token sits
+    # anywhere else (126 included) leaves its running state in the slot instead
+    rng = np.random.default_rng(24)
+    D = 128
+    ends = [125, 126, 127, 128, 129, 254, 255, 256, 383]  # sequence lengths around chunk ends
+    B = len(ends)
+    seq = np.array(ends, np.int64)
+    ext = np.array([int(rng.integers(1, e + 1)) for e in ends], np.int64)
+    T = int(ext.sum())
+    inp = rng.standard_normal((T, 2 * D)).astype(np.float32)
+    ape = (rng.standard_normal((128, D)) * 0.1).astype(np.float32)
+    state = rng.standard_normal((B, 3, D)).astype(np.float32)
+    state[:, 1] = np.abs(state[:, 1]) + 1.0
+    out, w, fs, sw = ora.c128_prefill(state, inp, ape, np.arange(B), seq, ext)
+    pos = np.concatenate([np.arange(s - e, s) for s, e in zip(seq, ext)])
+    w, sw = w.astype(bool), sw.astype(bool)
+    np.testing.assert_array_equal(w, pos % 128 == 127)
+    np.testing.assert_array_equal(sw, (seq - 1) % 128 != 127)
+    # the values go where the flags say: emitted rows and stored states are
+    # finite, rows of tokens that emit nothing are left unwritten (NaN)
+    assert np.all(np.isfinite(out[w])) and np.all(np.isnan(out[~w]))
+    assert np.all(np.isfinite(fs[sw]))
 
 
 def test_c128_prefill_single_token_window(ora):
