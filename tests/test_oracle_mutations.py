@@ -82,6 +82,9 @@ MUTANTS = [
     ("pooled decode stashes at the tail slot's own offset",
      "std::memcpy(kring + slot * D, kcur, D * 2);",
      "std::memcpy(kring + (std::max(tslot, 0) % P) * D, kcur, D * 2);"),
+    ("c128 FP8 store: the row enters the rotation without its bf16 rounding",
+     "for (int d = 0; d < 128; ++d) xf[d] = bf16_to_float(bf16_from_double(rows[r * D + 128 * j + d]));",
+     "for (int d = 0; d < 128; ++d) xf[d] = static_cast<float>(rows[r * D + 128 * j + d]);"),
     ("c128 FP8 store: block scales laid out block-major",
      "std::memcpy(base + page_size * D + 4 * (tok * blocks + j), &scale, 4);",
      "std::memcpy(base + page_size * D + 4 * (j * page_size + tok), &scale, 4);"),

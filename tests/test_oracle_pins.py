@@ -988,6 +988,25 @@ def test_c128_rows_to_cache_golden(ora, round_scale):
     np.testing.assert_array_equal(cache, before)
 
 
+def test_c128_rows_to_cache_rounds_the_row_to_bf16_first(ora):
+    """Worked by hand, D = 128, power-of-two scale: the row (1, 1 - 2^-9, 0,
+    ..., 0) rounds to bf16 (1, 1) (1 - 2^-9 is a tie between 1 - 2^-8 and 1;
+    1 has the even mantissa), so the rotation is 2c in even channels and 0 in
+    odd ones (c = fp32(1/sqrt(128))).  bf16(2c) = 0.1767578125 is the absmax;
+    absmax/448 = 3.95e-4 gives the scale 2^-11; 0.1767578125 * 2^11 = 362
+    rounds to the e4m3 value 352 = 1.375 * 2^8, code 0x7B; the odd channels are
+    +0, code 0x00.  Without the first rounding the odd channels would hold
+    2^-9 c and a nonzero code."""
+    D, ps = 128, 1
+    cache = np.full((1, ps, D + 4), 0xAB, np.uint8)
+    row = np.zeros((1, D), np.float32)
+    row[0, 0], row[0, 1] = 1.0, 1.0 - 2.0 ** -9
+    ora.c128_rows_to_cache(cache, ps, row, np.array([0]), round_scale=True)
+    codes = cache[0, 0, :D]
+    assert np.all(codes[0::2] == 0x7B) and np.all(codes[1::2] == 0x00)
+    assert cache[0, 0, D:].view(np.float32)[0] == 2.0 ** -11
+
+
 @pytest.mark.parametrize("round_scale", [False, True])
 def test_c128_rows_to_cache_inverse_rotation(ora, round_scale):
     """Decoding the codes, scaling them and applying the inverse of the
