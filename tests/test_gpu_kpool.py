@@ -158,6 +158,31 @@ def test_kpool_compress_vs_oracle(cvariant, ck, ora, P, round_scale):
     assert np.all(gcache.reshape(-1)[mask] == 0x5A), "bytes outside the written rows changed"
 
 
+def test_kpool_compress_worked_bf16_tie(cvariant, ck):
+    """The hand-worked pool of the oracle pins (P = 2, equal weights, keys (1, 1)
+    in channel 0 and (1, 1 - 2^-8) in channel 1): x = 1 - 2^-9 in channel 1 is
+    a bf16 tie that goes to 1, so the rotation gives 2c in even channels and 0
+    in odd ones; power-of-two scale 2^-11, codes 0x7B and 0x00.  On the GPU the
+    equal weights are ex2(0) = 1 exactly and the mean is exact, so the codes are
+    exact too."""
+    n, P = 3, 2  # three copies of the pool
+    k = torch.zeros((n, P, D))
+    k[:, :, 0] = 1.0
+    k[:, 1, 1] = 1.0 - 2.0 ** -8
+    z = torch.zeros((n, P, D), dtype=torch.bfloat16)
+    dev = "cuda"
+    out_q = torch.zeros((n, D), dtype=torch.uint8, device=dev)
+    out_s = torch.zeros((n,), dtype=torch.float32, device=dev)
+    err = torch.zeros((1,), dtype=torch.int32, device=dev)
+    ck.ckv_kpool_compress(k.to(torch.bfloat16).to(dev), z.to(dev), torch.zeros((P, D), device=dev),
+                          write_cache=False, out_fp8=out_q, out_scale=out_s, round_scale=True, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    q = u8(out_q)
+    assert np.all(q[:, 0::2] == 0x7B) and np.all(q[:, 1::2] == 0x00)
+    assert np.all(f32(out_s) == 2.0 ** -11)
+
+
 def test_kpool_compress_write_mask_and_cache_only(cvariant, ck, ora):
     n, P = 77, 16
     g = torch.Generator().manual_seed(7)

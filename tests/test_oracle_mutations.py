@@ -82,6 +82,11 @@ MUTANTS = [
     ("pooled decode stashes at the tail slot's own offset",
      "std::memcpy(kring + slot * D, kcur, D * 2);",
      "std::memcpy(kring + (std::max(tslot, 0) % P) * D, kcur, D * 2);"),
+    ("pooled path: the pool output enters the rotation without its bf16 rounding",
+     "  // D == 128 for the rotation (checked by the callers).\n  float xf[128], yf[128];\n"
+     "  for (int d = 0; d < 128; ++d) xf[d] = bf16_to_float(xb[d]);",
+     "  // D == 128 for the rotation (checked by the callers).\n  float xf[128], yf[128];\n"
+     "  for (int d = 0; d < 128; ++d) xf[d] = static_cast<float>(x[d]);"),
     ("c128 FP8 store: the row enters the rotation without its bf16 rounding",
      "for (int d = 0; d < 128; ++d) xf[d] = bf16_to_float(bf16_from_double(rows[r * D + 128 * j + d]));",
      "for (int d = 0; d < 128; ++d) xf[d] = static_cast<float>(rows[r * D + 128 * j + d]);"),

@@ -301,6 +301,25 @@ def test_pool_golden(ora, case):
         assert r2["q"][0] == case["linear"]["q0"]
 
 
+def test_pool_rotation_takes_the_bf16_rounded_output(ora):
+    """Worked by hand: P = 2 with equal weights (scores and bias 0), keys
+    (1, 1) in channel 0 and (1, 1 - 2^-8) in channel 1 (both bf16), zeros
+    elsewhere: x = (1, 1 - 2^-9, 0, ...), and 1 - 2^-9 is a bf16 tie between
+    1 - 2^-8 and 1 that goes to 1 (even mantissa), so xb = (1, 1, 0, ...).
+    The rotation of xb is 2c in even channels and 0 in odd ones (c =
+    fp32(1/sqrt(128))): yb even = bf16(2c) = 0.1767578125, power-of-two scale
+    2^-11, 0.1767578125 * 2^11 = 362 -> e4m3 352, code 0x7B; odd codes 0x00.
+    Rotating the unrounded x instead would leave 2^-9 c in the odd channels."""
+    k = np.zeros((2, 128), np.float32)
+    k[:, 0] = 1.0
+    k[0, 1], k[1, 1] = 1.0, 1.0 - 2.0 ** -8
+    z = np.zeros((2, 128), np.float32)
+    r = _pool(ora, k, z, z, True)
+    assert r["x"][1] == 1.0 - 2.0 ** -9 and r["xb"][1] == 0x3F80
+    assert np.all(r["yb"][1::2] == 0) and np.all(r["q"][0::2] == 0x7B) and np.all(r["q"][1::2] == 0x00)
+    assert r["scale"] == 2.0 ** -11
+
+
 def test_pool_equal_scores_give_mean(ora):
     rng = np.random.default_rng(8)
     for P in (1, 2, 4, 8, 16):
