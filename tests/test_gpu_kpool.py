@@ -168,7 +168,7 @@ def test_kpool_compress_worked_bf16_tie(cvariant, ck):
     n, P = 3, 2  # three copies of the pool
     k = torch.zeros((n, P, D))
     k[:, :, 0] = 1.0
-    k[:, 1, 1] = 1.0 - 2.0 ** -8
+    k[:, 0, 1], k[:, 1, 1] = 1.0, 1.0 - 2.0 ** -8
     z = torch.zeros((n, P, D), dtype=torch.bfloat16)
     dev = "cuda"
     out_q = torch.zeros((n, D), dtype=torch.uint8, device=dev)
