@@ -261,12 +261,19 @@ def kpool_seed_tail(ring, key, score, tslot):
 
 
 def expand_pools_and_append_tail(pool_ids, seq_lens, P):
-    """[KPOOL] pool -> token index expansion with the tail appended; int32 [rows, G*P + P - 1]."""
-    pool_ids = np.ascontiguousarray(pool_ids, np.int32)
+    """[KPOOL] pool -> token index expansion with the tail appended; int32 [rows, G*P + P - 1].
+
+    pool_ids int32 [rows, G]: a row-strided view (contiguous rows of a wider
+    array) is passed with its own row stride."""
+    pool_ids = np.asarray(pool_ids)
+    if pool_ids.dtype != np.int32 or pool_ids.ndim != 2 or pool_ids.strides[1] != 4 or pool_ids.strides[0] % 4 \
+            or pool_ids.strides[0] < 4 * pool_ids.shape[1]:
+        pool_ids = np.ascontiguousarray(pool_ids, np.int32)
     seq_lens = np.ascontiguousarray(seq_lens, np.int64)
     rows, groups = pool_ids.shape
+    stride = pool_ids.strides[0] // 4 if rows > 1 else groups
     out = np.empty((rows, groups * P + P - 1), np.int32)
-    lib().ora_expand_pools_and_append_tail(_p(pool_ids, ctypes.c_int32), groups, _p(seq_lens, ctypes.c_int64),
+    lib().ora_expand_pools_and_append_tail(_p(pool_ids, ctypes.c_int32), stride, _p(seq_lens, ctypes.c_int64),
                                            rows, groups, P, _p(out, ctypes.c_int32))
     return out
 

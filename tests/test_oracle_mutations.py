@@ -90,6 +90,9 @@ MUTANTS = [
     ("c128 FP8 store: the row enters the rotation without its bf16 rounding",
      "for (int d = 0; d < 128; ++d) xf[d] = bf16_to_float(bf16_from_double(rows[r * D + 128 * j + d]));",
      "for (int d = 0; d < 128; ++d) xf[d] = static_cast<float>(rows[r * D + 128 * j + d]);"),
+    ("pool expansion reads the ids with the group count as row stride",
+     "const int64_t id = pool_ids[r * stride + g];",
+     "const int64_t id = pool_ids[r * groups + g];"),
     ("c128 FP8 store: block scales laid out block-major",
      "std::memcpy(base + page_size * D + 4 * (tok * blocks + j), &scale, 4);",
      "std::memcpy(base + page_size * D + 4 * (j * page_size + tok), &scale, 4);"),

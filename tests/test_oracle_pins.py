@@ -943,6 +943,13 @@ def test_segmenter_invariants_brute_force(ora):
 def test_expand_golden(ora, case):
     out = ora.expand_pools_and_append_tail(np.array(case["pool_ids"]), np.array(case["seq_lens"]), case["P"])
     assert out.tolist() == case["out"]
+    # the same ids as the first columns of wider rows (row stride G + 3, junk
+    # in the extra columns) give the same output
+    ids = np.array(case["pool_ids"], np.int32).reshape(len(case["seq_lens"]), -1)
+    wide = np.full((ids.shape[0], ids.shape[1] + 3), 12345, np.int32)
+    wide[:, :ids.shape[1]] = ids
+    out = ora.expand_pools_and_append_tail(wide[:, :ids.shape[1]], np.array(case["seq_lens"]), case["P"])
+    assert out.tolist() == case["out"]
 
 
 def test_expand_invariants(ora):
