@@ -116,14 +116,37 @@ def _run_pins(so):
                           cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
 
 
-def test_control_build_passes_the_pins(tmp_path):
-    r = _run_pins(_build(tmp_path, open(SRC).read(), "control"))
-    assert r.returncode == 0, r.stdout[-2000:]
+def _outcome(tmp_dir, name, source):
+    path = tmp_dir / name
+    path.mkdir()
+    r = _run_pins(_build(path, source, name))
+    return r.returncode, r.stdout[-1500:]
+
+
+@pytest.fixture(scope="module")
+def outcomes(tmp_path_factory):
+    """Every planted mistake (and the unchanged control) built and run against
+    the pins, several at a time; keyed by the mistake's description."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    src = open(SRC).read()
+    jobs = {"control": src}
+    for what, old, new in MUTANTS:
+        if src.count(old) == 1:
+            jobs[what] = src.replace(old, new)
+    tmp = tmp_path_factory.mktemp("mutants")
+    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+        futs = {what: ex.submit(_outcome, tmp, f"m{i}", source) for i, (what, source) in enumerate(jobs.items())}
+        return {what: f.result() for what, f in futs.items()}
+
+
+def test_control_build_passes_the_pins(outcomes):
+    rc, out = outcomes["control"]
+    assert rc == 0, out
 
 
 @pytest.mark.parametrize("what,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_catch_planted_mistake(tmp_path, what, old, new):
-    src = open(SRC).read()
-    assert src.count(old) == 1, f"the oracle no longer contains the mutated line: {old}"
-    r = _run_pins(_build(tmp_path, src.replace(old, new), "mutant"))
-    assert r.returncode == 1, f"the pins did not catch: {what}\n{r.stdout[-1500:]}"
+def test_pins_catch_planted_mistake(outcomes, what, old, new):
+    assert open(SRC).read().count(old) == 1, f"the oracle no longer contains the mutated line: {old}"
+    rc, out = outcomes[what]
+    assert rc == 1, f"the pins did not catch: {what}\n{out}"
