@@ -133,6 +133,47 @@ def test_decode_fp8(ck, ora, D, dtype, round_scale):
                          round_scale, f"c128 decode fp8 D={D} {dtype} round={round_scale}")
 
 
+@pytest.mark.parametrize("round_scale", [True, False])
+@pytest.mark.parametrize("closing", ["workload", "third"])
+def test_decode_fp8_full_size(ck, ora, closing, round_scale):
+    """The full-size decode batch (2048 requests, D = 512, fp32, 4096 slots)
+    in the launch the bench times (FP8 rows only, PDL): the requests' own
+    sequence lengths (about 16 closing), or a third of them closing.  States
+    equal the plain call's bit for bit; the cache holds exactly the oracle's
+    store of the GPU's rows (from a separate plain call) and every other byte
+    keeps its canary; end to end against the oracle's own rows."""
+    from compressed_kv_attention_gated_gb300 import synth
+
+    d = synth.c128_decode("cpu", seed=5)
+    B, D = d["B"], d["D"]
+    if closing == "third":
+        seq = d["seq_lens"].clone()
+        seq[::3] = (seq[::3] // 128 + 1) * 128
+        d["seq_lens"] = seq
+    closed = ((d["seq_lens"].numpy().astype(np.int64) - 1) % 128) == 127
+    cache0, ps = _cache(B, D, ps=64)
+    cache_loc = torch.randperm(cache0.shape[0] * ps, generator=torch.Generator().manual_seed(9))[:B].to(torch.int64)
+    dev = "cuda"
+    args = [d["input"].to(dev), None, d["ape"].to(dev), d["indices"].to(dev), d["seq_lens"].to(dev)]
+    st_p, out_p = d["state"].to(dev).clone(), torch.zeros((B, D), device=dev)
+    ck.ckv_c128_online_decode(st_p, args[0], out_p, *args[2:])
+    err = torch.zeros((1,), dtype=torch.int32, device=dev)
+    st_n, cache = d["state"].to(dev).clone(), cache0.to(dev)
+    ck.ckv_c128_online_decode_fp8(st_n, args[0], None, *args[2:], cache, cache_loc.to(dev),
+                                  round_scale=round_scale, use_pdl=True, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and closed.sum() >= 8
+    assert np.array_equal(f32(st_n).view(np.uint32), f32(st_p).view(np.uint32))
+    rows = f32(out_p)[closed]
+    np.testing.assert_array_equal(u8(cache), _expect(ora, cache0, ps, rows, cache_loc.numpy()[closed], round_scale))
+    out_ref, _, cl = ora.c128_decode(f32(d["state"]), _input_np(d["input"]), f32(d["ape"]), d["indices"].numpy(),
+                                     d["seq_lens"].numpy())
+    assert np.array_equal(cl, closed)
+    assert_close_rel(rows, out_ref[closed], "closing rows")
+    check_vs_oracle_rows(ora, u8(cache), cache0, ps, rows, out_ref[closed], cache_loc.numpy()[closed], round_scale,
+                         f"c128 decode fp8 full size closing={closing} round={round_scale}")
+
+
 def _prefill(ck, d, cp, wp, nc, nw, out, cache, cache_loc, round_scale, use_pdl, err, fp8=True):
     dev = "cuda"
     state = d["state"].to(dev).clone()
