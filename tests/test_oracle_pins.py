@@ -247,7 +247,7 @@ def _e4m3_nearest_code(t):
 
 @pytest.mark.parametrize("am_bits,y_bits", [(0x3F84, 0x3784), (0x3F98, 0x3798), (0x3FA3, 0x37A3)])
 def test_quantize_linear_scale_divides(ora, am_bits, y_bits):
-    """Reading 4: q = y / scale is one IEEE fp32 division.  The row holds its
+    """The quotient q = y / scale is one IEEE fp32 division.  The row holds its
     absmax a and one element y = a * 2^-16, so y / scale lies within an fp32
     ulp of the e4m3 midpoint 3.5 * 2^-9: fp32(y / scale) and fp32(y *
     fp32(1 / scale)) round to different codes.  The expected code and scale
