@@ -122,8 +122,29 @@ __device__ __forceinline__ void write_taps(float* tx, uint16_t* txb, uint16_t* t
         make_uint2(pack_bf16x2_rn(yb[0], yb[1]), pack_bf16x2_rn(yb[2], yb[3]));
 }
 
-__device__ __forceinline__ void cache_write(uint8_t* cache, int64_t page_size, int64_t loc,
-                                            int lane, uint32_t codes, float scale) {
+// Where cache row loc lives: its kD code bytes and its fp32 scale.  Computed
+// as soon as loc is known, so that the 64-bit division is off the path
+// between a pool's arithmetic and its store.
+struct CacheRow {
+  uint8_t* codes;
+  float* scale;
+};
+
+__device__ __forceinline__ CacheRow cache_row(uint8_t* cache, int64_t page_size, int64_t loc) {
+  const int64_t page = loc / page_size, tok = loc - page * page_size;
+  uint8_t* base = cache + page * page_size * kRowBytes;
+  return {base + tok * kD, reinterpret_cast<float*>(base + page_size * kD) + tok};
+}
+
+__device__ __forceinline__ void cache_write(const CacheRow& row, int lane, uint32_t codes, float scale) {
+  reinterpret_cast<uint32_t*>(row.codes)[lane] = codes;
+  if (lane == 0) *row.scale = scale;
+}
+
+// The same with the address formed at the store (the bulk pipeline: holding
+// the address across its wait costs registers and measured slower).
+__device__ __forceinline__ void cache_write(uint8_t* cache, int64_t page_size, int64_t loc, int lane,
+                                            uint32_t codes, float scale) {
   const int64_t page = loc / page_size, tok = loc - page * page_size;
   uint8_t* base = cache + page * page_size * kRowBytes;
   reinterpret_cast<uint32_t*>(base + tok * kD)[lane] = codes;
@@ -175,16 +196,18 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   }
   stage_ape<P>(s_ape, a.ape);
   if (!want) return;
+  const bool loc_ok = a.write_cache && loc >= 0 && loc < a.num_pages * a.page_size;
+  const CacheRow row = loc_ok ? cache_row(a.cache, a.page_size, loc) : CacheRow{nullptr, nullptr};
   float x[4], xb[4], yb[4], scale;
   uint32_t codes;
   pool_softmax<P>(kr, sr, s_ape, lane, x);
   rotate_quantize<kRound>(x, lane, codes, scale, xb, yb);
 
   if (a.write_cache) {
-    if (loc < 0 || loc >= a.num_pages * a.page_size) {
+    if (!loc_ok) {
       if (lane == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
     } else {
-      cache_write(a.cache, a.page_size, loc, lane, codes, scale);
+      cache_write(row, lane, codes, scale);
     }
   }
   if (a.out_fp8) {
@@ -419,7 +442,8 @@ __global__ void __launch_bounds__(kDecThreads)
 
   // the pool waiting for its arithmetic: its rows, bias, cache row and tap row
   bool pend = false;
-  int64_t pend_loc = 0, pend_row = 0;
+  int64_t pend_row = 0;
+  CacheRow pend_cache{nullptr, nullptr};
   uint32_t kr[P], sr[P];
   float2 ap[P];
   auto finish = [&]() {
@@ -451,10 +475,8 @@ __global__ void __launch_bounds__(kDecThreads)
     float xb[2], yb[2], scale;
     uint32_t codes;
     rotate_quantize_pair<kRound>(x0, x1, t, s_x, codes, scale, xb, yb);
-    const int64_t page = pend_loc / a.page_size, tok = pend_loc - page * a.page_size;
-    uint8_t* base = a.cache + page * a.page_size * kRowBytes;
-    reinterpret_cast<uint16_t*>(base + tok * kD)[t] = static_cast<uint16_t>(codes);
-    if (t == 0) *reinterpret_cast<float*>(base + a.page_size * kD + 4 * tok) = scale;
+    reinterpret_cast<uint16_t*>(pend_cache.codes)[t] = static_cast<uint16_t>(codes);
+    if (t == 0) *pend_cache.scale = scale;
     if (a.tap_x) reinterpret_cast<float2*>(a.tap_x + pend_row * kD)[t] = make_float2(x0, x1);
     if (a.tap_xb) reinterpret_cast<uint32_t*>(a.tap_xb + pend_row * kD)[t] = pack_bf16x2_rn(xb[0], xb[1]);
     if (a.tap_yb) reinterpret_cast<uint32_t*>(a.tap_yb + pend_row * kD)[t] = pack_bf16x2_rn(yb[0], yb[1]);
@@ -492,7 +514,7 @@ __global__ void __launch_bounds__(kDecThreads)
 #pragma unroll
           for (int j = 0; j < P; ++j) ap[j] = __ldg(reinterpret_cast<const float2*>(a.ape + j * kD) + t);
           pend = true;
-          pend_loc = loc[i];
+          pend_cache = cache_row(a.cache, a.page_size, loc[i]);
           pend_row = static_cast<int64_t>(b) * a.N + t0 + i;
         }
       }
