@@ -17,7 +17,8 @@
 //           warp, b0 = w rounded down to a multiple of 4 and kept inside idx)
 //           and 8 four-byte row words 256 bytes apart, and lane 0 stores the
 //           exclusive or of the 20 words it loaded.
-// An index outside [0, num_rows) is skipped.
+// Every load takes the read-only path (ld.global.nc), as the decode's own
+// index and row loads do.  An index outside [0, num_rows) is skipped.
 #include <cstdint>
 
 #include "ckv_device.cuh"
@@ -25,6 +26,10 @@
 
 namespace ckv {
 namespace {
+
+// x mod m for x >= 0, m > 0, with no division when x < m already (a 64-bit
+// division would add its own latency in front of the loads being measured)
+__device__ __forceinline__ int64_t wrap(int64_t x, int64_t m) { return x < m ? x : x % m; }
 
 template <int kHops>
 __global__ void latency_probe_kernel(const int32_t* idx, const uint2* rows, int64_t num_rows, uint2* out,
@@ -35,22 +40,22 @@ __global__ void latency_probe_kernel(const int32_t* idx, const uint2* rows, int6
     const int lane = threadIdx.x & 31;
     const int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (w >= n_warps) return;
-    const int32_t r = idx[w];
+    const int32_t r = __ldg(idx + w);
     if constexpr (kHops == 1) {
       if (lane == 0) reinterpret_cast<int32_t*>(out + w * 32)[0] = r;
     } else if constexpr (kHops == 2) {
       if (r < 0 || r >= num_rows) return;
-      out[w * 32 + lane] = rows[static_cast<int64_t>(r) * 32 + lane];
+      out[w * 32 + lane] = __ldg(rows + static_cast<int64_t>(r) * 32 + lane);
     } else {
       // n_warps >= 16 and num_rows >= 9 (checked by the caller): the 16 index
       // words and the 8 row words below stay inside idx and rows
       const int64_t b0 = min(w & ~int64_t{3}, static_cast<int64_t>(n_warps) - 16);
       int32_t acc = r;
 #pragma unroll
-      for (int q = 1; q < 12; ++q) acc ^= idx[b0 + ((q * 7) & 15)];
-      const uint32_t* rw = reinterpret_cast<const uint32_t*>(rows) + (w * 8) % (num_rows * 64 - 512) + lane;
+      for (int q = 1; q < 12; ++q) acc ^= __ldg(idx + b0 + ((q * 7) & 15));
+      const uint32_t* rw = reinterpret_cast<const uint32_t*>(rows) + wrap(w * 8, num_rows * 64 - 512) + lane;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc ^= static_cast<int32_t>(rw[q * 64]);
+      for (int q = 0; q < 8; ++q) acc ^= static_cast<int32_t>(__ldg(rw + q * 64));
       if (lane == 0) reinterpret_cast<int32_t*>(out + w * 32)[0] = acc;
     }
   }
