@@ -336,7 +336,8 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 1)
 // walked in order, kPrefetch at a time; all 64 threads load the group's index
 // words (the same words: broadcast) and their pair of the group's key and
 // score rows.  A closing pool's ring rows and bias are loaded together (the
-// one round trip that depends on the index words); its arithmetic is
+// one round trip that depends on the index words) and its cache row is
+// located while they are in flight; its arithmetic is
 // deferred until the stashes of the later tokens of the group (or, after the
 // last group, of the request) have been issued, so those stores are not left
 // at the end of the critical path.  A thread's later store to a ring slot
