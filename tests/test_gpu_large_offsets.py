@@ -141,3 +141,89 @@ def test_kpool_decode_ring_and_cache_past_2_31(ck, ora, round_scale):
     n_closing, _ = _compare_decode(ora, d, gpu, _oracle_decode(ora, d, round_scale), round_scale,
                                    f"pooled decode at large offsets round={round_scale}")
     assert n_closing > 0
+
+
+@pytest.mark.parametrize("variant", [1, 2], ids=["warp_per_pool", "bulk_pipeline"])
+def test_kpool_compress_pools_past_2_31_elements(ck, ora, variant):
+    """2^20 + 4096 one-shot pools (4.3 GB of keys, the same of scores): the
+    rows of pools past 2^20 start past element 2^31.  Sampled pools at the
+    top and the bottom against the oracle, stage by stage (as in the ordinary
+    one-shot tests)."""
+    from test_gpu_kpool import D, check_rows
+    from helpers import bf16_bits
+
+    P = 16
+    n = (1 << 20) + 4096
+    g = torch.Generator(device="cuda")
+    g.manual_seed(34)
+    dev = "cuda"
+    slot_k = torch.randn((n, P, D), generator=g, device=dev, dtype=torch.bfloat16)
+    slot_s = torch.randn((n, P, D), generator=g, device=dev, dtype=torch.bfloat16) * 2
+    ape = torch.randn((P, D), generator=g, device=dev) * 0.1
+    out_q = torch.zeros((n, D), dtype=torch.uint8, device=dev)
+    out_s = torch.zeros((n,), dtype=torch.float32, device=dev)
+    tx = torch.zeros((n, D), device=dev)
+    txb = torch.zeros((n, D), dtype=torch.bfloat16, device=dev)
+    tyb = torch.zeros((n, D), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros((1,), dtype=torch.int32, device=dev)
+    prev = ck.ckv_kpool_compress_set_variant(variant)
+    try:
+        ck.ckv_kpool_compress(slot_k, slot_s, ape, write_cache=False, out_fp8=out_q, out_scale=out_s, tap_x=tx,
+                              tap_xb=txb, tap_yb=tyb, err_word=err)
+        torch.cuda.synchronize()
+    finally:
+        ck.ckv_kpool_compress_set_variant(prev)
+    assert int(err.item()) == 0
+    pick = torch.cat([torch.arange(8), torch.randperm(n - (1 << 20), generator=torch.Generator().manual_seed(35))[:40]
+                      + (1 << 20), torch.tensor([n - 1])]).to(dev)
+    sk, ss = bf16_bits(slot_k[pick]), bf16_bits(slot_s[pick])
+    gx, gxb, gyb = f32(tx[pick]), bf16_bits(txb[pick]), bf16_bits(tyb[pick])
+    gq, gs = out_q[pick].cpu().numpy(), f32(out_s[pick])
+    ape_h = f32(ape)
+    del slot_k, slot_s, out_q, out_s, tx, txb, tyb
+    _free()
+    m = len(pick)
+    ref = ora.kpool_compress(np.zeros((1, 1, D + 4), np.uint8), 1, sk, ss, ape_h, np.zeros(m, np.int64),
+                             write_cache=False, return_compressed=True, taps=True)
+    check_rows(ora, gx, gxb, gyb, gq, gs, ref, True, f"one-shot pools past 2^31 variant={variant}")
+
+
+@pytest.mark.parametrize("variant", [1, 2], ids=["cta_per_segment", "tma_pipeline"])
+def test_c128_prefill_tokens_past_2_31_elements(ck, ora, variant):
+    """One request of 2^21 + 2^17 bf16 tokens from position 0 (a 4.6 GB
+    input: the rows past token 2^21 start past element 2^31).  Every chunk is
+    a whole compress segment, so each sampled row is the oracle's two-pass
+    over its own 128 tokens."""
+    from compressed_kv_attention_gated_gb300 import synth
+    from helpers import bf16_bits
+
+    D = 512
+    T = (1 << 21) + (1 << 17)
+    d = synth.c128_prefill("cuda", seed=36, B=1, D=D, max_extend=T, zero_prefix=True, num_slots=1,
+                           dtype=torch.bfloat16, score_dist="student_t")
+    assert d["num_tokens"] == T
+    cp, wp, nc, nw = ck.ckv_plan_online_prefill(d["seq_lens"].cpu(), d["extend_lens"].cpu())
+    assert nc == T // 128 and nw == 0
+    out = torch.full((T, D), -7.0, device="cuda")
+    err = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    prev = ck.ckv_c128_prefill_set_variant(variant)
+    try:
+        ck.ckv_c128_online_prefill(d["state"], d["input"], out, d["ape"], d["indices"], cp.cuda(), nc, wp.cuda(), nw,
+                                   use_pdl=True, err_word=err)
+        torch.cuda.synchronize()
+    finally:
+        ck.ckv_c128_prefill_set_variant(prev)
+    assert int(err.item()) == 0
+    chunks = torch.cat([torch.arange(4), torch.randperm(T // 128 - (1 << 14),
+                                                        generator=torch.Generator().manual_seed(37))[:24] + (1 << 14),
+                        torch.tensor([T // 128 - 1])])
+    ape = f32(d["ape"])
+    zero = np.zeros((1, 3, D), np.float32)
+    for c in chunks.tolist():
+        rows = d["input"][128 * c:128 * c + 128]
+        ref, w, _, _ = ora.c128_prefill(zero, bf16_bits(rows), ape, np.zeros(1, np.int32), np.array([128]),
+                                        np.array([128]))
+        assert w[127] and not w[:127].any()
+        assert_close_rel(f32(out[128 * c + 127])[None], ref[127][None], f"chunk {c}")
+    written = (out.view(T // 128, 128, D)[:, :127] != -7.0).any()
+    assert not bool(written), "rows other than the chunk ends were written"
