@@ -227,3 +227,58 @@ def test_c128_prefill_tokens_past_2_31_elements(ck, ora, variant):
         assert_close_rel(f32(out[128 * c + 127])[None], ref[127][None], f"chunk {c}")
     written = (out.view(T // 128, 128, D)[:, :127] != -7.0).any()
     assert not bool(written), "rows other than the chunk ends were written"
+
+
+def test_kpool_seed_tail_tokens_and_blocks_past_2_31(ck, ora):
+    """2^24 padded prefill tokens (tail slot -1) in front of a small seed
+    problem, whose key and score rows then start at element 2^31, with its
+    tail blocks shifted to 2^19 and up (ring element offset 2^31 and up)."""
+    from test_gpu_kpool import D, _seed_case
+    from helpers import bf16_bits
+
+    P = 16
+    lens = [37, 5, 300, 16, 1, 129]
+    tslot, key, score, ring0 = _seed_case(P, lens, 38)
+    base_tok, base_block = 1 << 24, 1 << 19
+    n = tslot.numel()
+    dev = "cuda"
+    big_ts = torch.full((base_tok + n,), -1, dtype=torch.int32, device=dev)
+    big_ts[base_tok:] = torch.where(tslot >= 0, tslot + base_block * P, tslot).to(dev)
+    big_key = torch.empty((base_tok + n, D), dtype=torch.bfloat16, device=dev)  # 4.3 GB, read only at the end
+    big_score = torch.empty((base_tok + n, D), dtype=torch.bfloat16, device=dev)
+    big_key[base_tok:] = key.to(dev)
+    big_score[base_tok:] = score.to(dev)
+    ring = torch.zeros((base_block + len(lens), 2, P, D), dtype=torch.bfloat16, device=dev)
+    ring[base_block:] = ring0.to(dev)
+    err = torch.zeros((1,), dtype=torch.int32, device=dev)
+    ck.ckv_kpool_seed_tail(ring, big_key, big_score, big_ts, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert not bool(ring[:base_block].view(torch.int16).any()), "ring blocks below the shifted ones were written"
+    got = bf16_bits(ring[base_block:])
+    del big_key, big_score, ring
+    _free()
+    rring = bf16_bits(ring0).copy()
+    ora.kpool_seed_tail(rring, bf16_bits(key), bf16_bits(score), tslot.numpy())
+    np.testing.assert_array_equal(got, rring)
+
+
+def test_expand_output_past_2_31_elements(ck, ora):
+    """65,600 rows of 2048 pool ids with P = 16: an 8.6 GB output whose rows
+    from row 65,507 on start past element 2^31.  Sampled rows against the
+    oracle."""
+    rows, groups, P = 65600, 2048, 16
+    g = torch.Generator(device="cuda")
+    g.manual_seed(39)
+    ids = torch.randint(-1, 1 << 20, (rows, groups), generator=g, device="cuda", dtype=torch.int32)
+    seq = torch.randint(0, groups * P + P, (rows,), generator=g, device="cuda", dtype=torch.int64)
+    out = ck.ckv_expand_pools_and_append_tail(ids, seq, P)
+    torch.cuda.synchronize()
+    cols = groups * P + P - 1
+    assert (rows - 1) * cols > 2 ** 31
+    pick = torch.cat([torch.arange(4), torch.arange(rows - 96, rows)]).to("cuda")
+    got = out[pick].cpu().numpy()
+    del out
+    _free()
+    ref = ora.expand_pools_and_append_tail(ids[pick].cpu().numpy(), seq[pick].cpu().numpy(), P)
+    np.testing.assert_array_equal(got, ref)
