@@ -26,6 +26,15 @@ ckv_status cuda_status(cudaError_t e) {
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// log2(n) for a power of two n > 0, else -1 (lets the kernels split a cache
+// location into page and row with a shift instead of a 64-bit division)
+int32_t pow2_shift(int64_t n) {
+  if (n <= 0 || (n & (n - 1)) != 0) return -1;
+  int32_t s = 0;
+  while ((int64_t{1} << s) != n) ++s;
+  return s;
+}
 bool pool_size_ok(int32_t P) { return P == 1 || P == 2 || P == 4 || P == 8 || P == 16; }
 bool head_dim_ok(int32_t D) { return D == 128 || D == 256 || D == 512; }
 
@@ -146,6 +155,7 @@ ckv_status ckv_kpool_compress(uint8_t* kv_cache, int64_t num_pages, int32_t page
   a.cache = kv_cache;
   a.num_pages = num_pages;
   a.page_size = page_size > 0 ? page_size : 1;
+  a.page_shift = pow2_shift(a.page_size);
   a.slot_k = slot_k;
   a.slot_score = slot_score;
   a.ape = ape;

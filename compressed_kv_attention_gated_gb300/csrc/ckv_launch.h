@@ -28,6 +28,7 @@ struct KpoolCompressArgs {
   int32_t* err;
   int64_t n_pools;
   int32_t write_cache;
+  int32_t page_shift;  // log2(page_size) when page_size is a power of two, else -1
 };
 
 struct KpoolDecodeArgs {

@@ -130,8 +130,14 @@ struct CacheRow {
   float* scale;
 };
 
-__device__ __forceinline__ CacheRow cache_row(uint8_t* cache, int64_t page_size, int64_t loc) {
-  const int64_t page = loc / page_size, tok = loc - page * page_size;
+// page = loc / page_size, by a shift when page_size is a power of two
+// (page_shift >= 0): a 64-bit division is a long instruction sequence
+__device__ __forceinline__ int64_t page_of(int64_t loc, int64_t page_size, int32_t page_shift) {
+  return page_shift >= 0 ? (loc >> page_shift) : loc / page_size;
+}
+
+__device__ __forceinline__ CacheRow cache_row(uint8_t* cache, int64_t page_size, int32_t page_shift, int64_t loc) {
+  const int64_t page = page_of(loc, page_size, page_shift), tok = loc - page * page_size;
   uint8_t* base = cache + page * page_size * kRowBytes;
   return {base + tok * kD, reinterpret_cast<float*>(base + page_size * kD) + tok};
 }
@@ -143,9 +149,9 @@ __device__ __forceinline__ void cache_write(const CacheRow& row, int lane, uint3
 
 // The same with the address formed at the store (the bulk pipeline: holding
 // the address across its wait costs registers and measured slower).
-__device__ __forceinline__ void cache_write(uint8_t* cache, int64_t page_size, int64_t loc, int lane,
-                                            uint32_t codes, float scale) {
-  const int64_t page = loc / page_size, tok = loc - page * page_size;
+__device__ __forceinline__ void cache_write(uint8_t* cache, int64_t page_size, int32_t page_shift, int64_t loc,
+                                            int lane, uint32_t codes, float scale) {
+  const int64_t page = page_of(loc, page_size, page_shift), tok = loc - page * page_size;
   uint8_t* base = cache + page * page_size * kRowBytes;
   reinterpret_cast<uint32_t*>(base + tok * kD)[lane] = codes;
   if (lane == 0) *reinterpret_cast<float*>(base + page_size * kD + 4 * tok) = scale;
@@ -197,7 +203,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   stage_ape<P>(s_ape, a.ape);
   if (!want) return;
   const bool loc_ok = a.write_cache && loc >= 0 && loc < a.num_pages * a.page_size;
-  const CacheRow row = loc_ok ? cache_row(a.cache, a.page_size, loc) : CacheRow{nullptr, nullptr};
+  const CacheRow row = loc_ok ? cache_row(a.cache, a.page_size, a.page_shift, loc) : CacheRow{nullptr, nullptr};
   float x[4], xb[4], yb[4], scale;
   uint32_t codes;
   pool_softmax<P>(kr, sr, s_ape, lane, x);
@@ -311,7 +317,7 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 1)
         if (loc < 0 || loc >= a.num_pages * a.page_size) {
           if (lane == 0) flag_error(a.err, CKV_DEVERR_CACHE_LOC);
         } else {
-          cache_write(a.cache, a.page_size, loc, lane, codes, scale);
+          cache_write(a.cache, a.page_size, a.page_shift, loc, lane, codes, scale);
         }
       }
       if (a.out_fp8) {
@@ -515,7 +521,8 @@ __global__ void __launch_bounds__(kDecThreads)
 #pragma unroll
           for (int j = 0; j < P; ++j) ap[j] = __ldg(reinterpret_cast<const float2*>(a.ape + j * kD) + t);
           pend = true;
-          pend_cache = cache_row(a.cache, a.page_size, loc[i]);
+          // the division overlaps the ring read here; a shift measured slower
+          pend_cache = cache_row(a.cache, a.page_size, -1, loc[i]);
           pend_row = static_cast<int64_t>(b) * a.N + t0 + i;
         }
       }

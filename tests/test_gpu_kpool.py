@@ -158,6 +158,54 @@ def test_kpool_compress_vs_oracle(cvariant, ck, ora, P, round_scale):
     assert np.all(gcache.reshape(-1)[mask] == 0x5A), "bytes outside the written rows changed"
 
 
+@pytest.mark.parametrize("ps", [1, 48, 100])
+def test_kpool_page_sizes(cvariant, ck, ora, ps):
+    """Cache pages of 1 row (a shift by 0) and of 48 or 100 rows (not powers of
+    two: the kernels divide instead of shifting): the one-shot rows against the
+    oracle stage by stage, each stored exactly at its location's page and row
+    with every other byte untouched; the decode with the same page size."""
+    from compressed_kv_attention_gated_gb300 import synth
+
+    n, P = 777, 16
+    g = torch.Generator().manual_seed(ps)
+    slot_k = torch.randn((n, P, D), generator=g).to(torch.bfloat16)
+    slot_s = torch.randn((n, P, D), generator=g).to(torch.bfloat16)
+    ape = torch.randn((P, D), generator=g) * 0.1
+    pages = (n + ps - 1) // ps + 2
+    loc = torch.randperm(pages * ps, generator=g)[:n].to(torch.int64)
+    cache0 = torch.full((pages, ps, D + 4), 0x5A, dtype=torch.uint8)
+    dev = "cuda"
+    cache = cache0.to(dev)
+    out_q = torch.zeros((n, D), dtype=torch.uint8, device=dev)
+    out_s = torch.zeros((n,), dtype=torch.float32, device=dev)
+    tx = torch.zeros((n, D), device=dev)
+    txb = torch.zeros((n, D), dtype=torch.bfloat16, device=dev)
+    tyb = torch.zeros((n, D), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros((1,), dtype=torch.int32, device=dev)
+    ck.ckv_kpool_compress(slot_k.to(dev), slot_s.to(dev), ape.to(dev), kv_cache=cache, loc=loc.to(dev),
+                          out_fp8=out_q, out_scale=out_s, tap_x=tx, tap_xb=txb, tap_yb=tyb, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = ora.kpool_compress(u8(cache0).copy(), ps, bf16_bits(slot_k), bf16_bits(slot_s), f32(ape), loc.numpy(),
+                             return_compressed=True, taps=True)
+    gq, gs = u8(out_q), f32(out_s)
+    check_rows(ora, f32(tx), bf16_bits(txb), bf16_bits(tyb), gq, gs, ref, True, f"one-shot page_size={ps}")
+    gcache = u8(cache)
+    cq, cs = cache_rows(gcache, ps, D, loc.numpy())
+    np.testing.assert_array_equal(cq, gq)
+    np.testing.assert_array_equal(cs.view(np.uint32), gs.view(np.uint32))
+    rest = gcache.reshape(-1).copy()
+    for l in loc.numpy():
+        page, tok = divmod(int(l), ps)
+        base = page * ps * (D + 4)
+        rest[base + tok * D: base + tok * D + D] = 0x5A
+        rest[base + ps * D + 4 * tok: base + ps * D + 4 * tok + 4] = 0x5A
+    assert np.all(rest == 0x5A), "bytes outside the written rows changed"
+    d = synth.pooled_decode("cpu", seed=ps, B=64, max_start=2048, page_size=ps)
+    gpu = _run_decode(ck, d, True)
+    _compare_decode(ora, d, gpu, _oracle_decode(ora, d, True), True, f"decode page_size={ps}")
+
+
 def test_kpool_compress_worked_bf16_tie(cvariant, ck):
     """The hand-worked pool of the oracle pins (P = 2, equal weights, keys (1, 1)
     in channel 0 and (1, 1 - 2^-8) in channel 1): x = 1 - 2^-9 in channel 1 is
