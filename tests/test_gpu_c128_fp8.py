@@ -174,6 +174,45 @@ def test_decode_fp8_full_size(ck, ora, closing, round_scale):
                          f"c128 decode fp8 full size closing={closing} round={round_scale}")
 
 
+@pytest.mark.parametrize("ps", [1, 48])
+def test_fp8_page_sizes(variant, ck, ora, ps):
+    """Cache pages of 1 row (a shift by 0) and of 48 rows (not a power of two:
+    the page comes from a division): decode and prefill rows stored exactly
+    where the oracle's store of the GPU's own rows puts them."""
+    from compressed_kv_attention_gated_gb300 import synth
+
+    D, B = 512, 301
+    d = synth.c128_decode("cpu", seed=40 + ps, B=B, D=D, num_slots=700)
+    seq = d["seq_lens"].clone()
+    seq[::3] = (seq[::3] // 128 + 1) * 128
+    d["seq_lens"] = seq
+    closed = ((seq.numpy().astype(np.int64) - 1) % 128) == 127
+    cache0, ps = _cache(B, D, ps=ps)
+    cache_loc = torch.randperm(cache0.shape[0] * ps, generator=torch.Generator().manual_seed(ps))[:B].to(torch.int64)
+    dev = "cuda"
+    args = [d["input"].to(dev), None, d["ape"].to(dev), d["indices"].to(dev), d["seq_lens"].to(dev)]
+    out = torch.zeros((B, D), device=dev)
+    err = torch.zeros((1,), dtype=torch.int32, device=dev)
+    cache = cache0.to(dev)
+    ck.ckv_c128_online_decode_fp8(d["state"].to(dev).clone(), args[0], out, *args[2:], cache, cache_loc.to(dev),
+                                  err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and closed.sum() > 50
+    np.testing.assert_array_equal(u8(cache), _expect(ora, cache0, ps, f32(out)[closed], cache_loc.numpy()[closed],
+                                                     True))
+    dp = synth.c128_prefill("cpu", seed=50 + ps, B=11, D=D, max_prefix=700, max_extend=900)
+    T = dp["num_tokens"]
+    cp, wp, nc, nw = ck.ckv_plan_online_prefill(dp["seq_lens"], dp["extend_lens"])
+    rows = cp[:nc].view(torch.int32).view(-1, 4)[:, 0].numpy().astype(np.int64)
+    cache0, _ = _cache(T, D, ps=ps)
+    cache_loc = torch.randperm(cache0.shape[0] * ps, generator=torch.Generator().manual_seed(ps + 1))[:T].to(torch.int64)
+    out_p, cache = torch.zeros((T, D), device=dev), cache0.to(dev)
+    _prefill(ck, dp, cp, wp, nc, nw, out_p, cache, cache_loc, True, True, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and nc > 10
+    np.testing.assert_array_equal(u8(cache), _expect(ora, cache0, ps, f32(out_p)[rows], cache_loc.numpy()[rows], True))
+
+
 def _prefill(ck, d, cp, wp, nc, nw, out, cache, cache_loc, round_scale, use_pdl, err, fp8=True):
     dev = "cuda"
     state = d["state"].to(dev).clone()
