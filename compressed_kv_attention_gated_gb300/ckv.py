@@ -164,9 +164,20 @@ def _stream(stream, ref):
 
 
 def _cuda(name, *ts):
+    """Every tensor on one CUDA device, the current one: the kernels run on the
+    current device, and a pointer into another device's memory would fault."""
+    devs = set()
     for t in ts:
-        if t is not None and not t.is_cuda:
+        if t is None:
+            continue
+        if not t.is_cuda:
             raise ValueError(f"{name}: every tensor must be on a CUDA device")
+        devs.add(t.device.index)
+    if len(devs) > 1:
+        raise ValueError(f"{name}: tensors on several CUDA devices {sorted(devs)}")
+    if devs and devs.pop() != torch.cuda.current_device():
+        raise ValueError(f"{name}: the tensors are not on the current CUDA device "
+                         f"(torch.cuda.set_device or torch.cuda.device(...) first)")
 
 
 def _check(func, status):

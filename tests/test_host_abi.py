@@ -169,3 +169,26 @@ def test_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError):
         ckv.ckv_c128_online_decode(torch.zeros((4, 3, 128)), x, torch.zeros((4, 128)), torch.zeros((128, 128)),
                                    torch.zeros(4, dtype=torch.int32), torch.ones(4, dtype=torch.int32))
+
+
+def test_binding_rejects_tensors_off_the_current_device(monkeypatch):
+    """The binding refuses tensors spread over several CUDA devices, or on a
+    device other than the current one, before anything reaches the library (a
+    kernel on one device given another device's pointers would fault)."""
+    import types
+
+    import torch
+
+    from compressed_kv_attention_gated_gb300 import ckv
+
+    def fake(index):
+        return types.SimpleNamespace(is_cuda=True, device=types.SimpleNamespace(index=index))
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    ckv._cuda("f", fake(0), None, fake(0))  # one device, the current one
+    with pytest.raises(ValueError, match="several CUDA devices"):
+        ckv._cuda("f", fake(0), fake(1))
+    with pytest.raises(ValueError, match="not on the current CUDA device"):
+        ckv._cuda("f", fake(1), fake(1))
+    with pytest.raises(ValueError, match="must be on a CUDA device"):
+        ckv._cuda("f", torch.zeros(1))
