@@ -408,8 +408,8 @@ ckv_status ckv_check_distinct(const void* ids, int32_t id_bytes, int64_t n, int6
  * ckv_check_distinct without a scratch argument, for callers that cannot
  * allocate device memory: e.g. a serving engine that has reserved nearly all
  * HBM for its paged KV cache and hands out no other buffers, or a loop that
- * must not call cudaMalloc because it may synchronise the device.  The paper
- * has no counterpart.  The bitmap is a static device array of
+ * must not call cudaMalloc because it may synchronise the device.  No source
+ * page describes this check (a debugging aid).  The bitmap is a static device array of
  * CKV_NOALLOC_MAX_RANGE bits (256 KB) inside the library, held by every GPU
  * that loads it until the process exits; the library allocates nothing.
  *   ids, id_bytes, n, err_word, stream  as for ckv_check_distinct
