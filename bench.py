@@ -1178,6 +1178,7 @@ def main():
         for name, case, rs in (("kpool_decode_update", "kpool_decode", True),
                                ("kpool_decode_update_linear_scale", "kpool_decode", False),
                                ("c128_online_decode", "c128_decode", True),
+                               ("c128_online_decode_fp8", "c128_decode_fp8", True),
                                ("latency_floor_2hops", "latency_floor2", True),
                                ("latency_floor_0hops", "latency_floor0", True)):
             r = rotation_timings(case, round_scale=rs)
@@ -1194,7 +1195,8 @@ def main():
         decode_cold["method"] = ("R instances (R x bytes per call >= 4 x L2, R >= 64), one call on each, captured in order "
                                  "in one CUDA graph with programmatic dependent launch; median of 100 replays / R. "
                                  "c128 decode: every state pool restored from a pristine copy and a 2 x L2 buffer "
-                                 "written before each replay (outside the events). latency_floor: the probe "
+                                 "written before each replay (outside the events); the fp8 entry stores FP8 rows "
+                                 "instead of fp32 rows. latency_floor: the probe "
                                  "kernels in the pooled decode's launch shape (512 warps, 4 per CTA), L2 flushed "
                                  "before each replay")
 
