@@ -776,7 +776,9 @@ def rotation_timings(case, replays=100, warmup=20, round_scale=True, instances=N
     decode's cold time.  latency_floor<h>_r<rows> draws the second hop's rows
     from a buffer of <rows> x 256 B (default 512 rows); latency_floor3 is one
     round trip with the pooled decode's own first-hop loads (512 warps or more,
-    9 rows or more).
+    9 rows or more); latency_floor4 the pooled decode's whole memory pattern
+    without its arithmetic (64 rows or more; _r16384 gives the second hop a
+    4 MB buffer like the ring).
 
     instances: a fixed instance count instead of the L2-sized one, with an L2
     flush before every replay (data cold, the instances' pages recently used)."""
@@ -860,12 +862,13 @@ def rotation_timings(case, replays=100, warmup=20, round_scale=True, instances=N
         def make(r):
             return {"idx": torch.randperm(nrows, generator=g, device=dev)[:n].to(torch.int32),
                     "rows": torch.randint(0, 255, (nrows, 256), generator=g, device=dev, dtype=torch.uint8),
-                    "out": torch.zeros((n, 256), device=dev, dtype=torch.uint8)}
+                    "out": torch.zeros(((4 if hops == 4 else 1) * n, 256), device=dev, dtype=torch.uint8)}
 
         def call(d, pdl):
             ck.ckv_latency_probe(hops, n, d["idx"], d["rows"], d["out"], warps_per_cta=wpc, use_pdl=pdl)
 
-        nbytes = {0: 0, 1: n * 8, 2: n * 516, 3: n * (48 + 1024 + 4)}[hops]
+        nbytes = {0: 0, 1: n * 8, 2: n * 516, 3: n * (48 + 1024 + 4),
+                  4: n * (48 + 1024 + 1024 + 4) + (n // 4) * 3840}[hops]
     else:
         raise SystemExit("--rotate applies to --case c128_decode, c128_decode_fp8, kpool_decode or latency_floor<h>")
     if instances:

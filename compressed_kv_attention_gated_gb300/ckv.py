@@ -611,9 +611,11 @@ def ckv_check_distinct_noalloc(ids, id_range, err_word, stream=None):
 
 def ckv_latency_probe(hops, n_warps, idx=None, rows=None, out=None, warps_per_cta=4, use_pdl=False, stream=None):
     """Latency floor of a decode-sized launch (see include/ckv.h): hops 0, 1 or
-    2 dependent global round trips per warp, or 3 for one round trip with the
-    pooled decode's first-hop loads.  idx int32 [n_warps]; rows and out uint8
-    [*, 256]; stream defaults to the current stream."""
+    2 dependent global round trips per warp, 3 for one round trip with the
+    pooled decode's first-hop loads, 4 for the pooled decode's memory pattern
+    without its arithmetic.  idx int32 [n_warps]; rows and out uint8 [*, 256]
+    (out: n_warps rows, 4 * n_warps for hops 4); stream defaults to the current
+    stream."""
     L = load()
     _cuda("ckv_latency_probe", idx, rows, out)
     if idx is not None:
@@ -623,7 +625,7 @@ def ckv_latency_probe(hops, n_warps, idx=None, rows=None, out=None, warps_per_ct
             _need(t.dtype == torch.uint8 and t.is_contiguous() and t.dim() == 2 and t.shape[1] == 256,
                   "rows/out must be contiguous uint8 [n, 256]")
     if out is not None:
-        _need(out.shape[0] >= n_warps, "out must have n_warps rows")
+        _need(out.shape[0] >= (4 if hops == 4 else 1) * n_warps, "out must have n_warps rows (4 n_warps for hops 4)")
     num_rows = rows.shape[0] if rows is not None else 0
     if stream is None:
         stream = torch.cuda.current_stream()

@@ -489,10 +489,11 @@ ckv_status ckv_check_distinct_noalloc(const void* ids, int32_t id_bytes, int64_t
 
 ckv_status ckv_latency_probe(int32_t hops, const int32_t* idx, const void* rows, int64_t num_rows, void* out,
                              int32_t n_warps, int32_t warps_per_cta, int32_t use_pdl, void* stream) {
-  if (hops < 0 || hops > 3 || n_warps < 1 || n_warps > (1 << 30) || warps_per_cta < 1 || warps_per_cta > 32 ||
+  if (hops < 0 || hops > 4 || n_warps < 1 || n_warps > (1 << 30) || warps_per_cta < 1 || warps_per_cta > 32 ||
       num_rows < 0)
     return CKV_ERR_SHAPE;
   if (hops == 3 && (n_warps < 16 || num_rows < 9)) return CKV_ERR_SHAPE;
+  if (hops == 4 && (n_warps < 16 || num_rows < 64)) return CKV_ERR_SHAPE;
   if (hops >= 1 && (!idx || !out)) return CKV_ERR_NULL;
   if (hops >= 2 && !rows) return CKV_ERR_NULL;
   if (!aligned(idx, 4) || !aligned(rows, 8) || !aligned(out, 8)) return CKV_ERR_ALIGN;

@@ -17,6 +17,17 @@
 //           warp, b0 = w rounded down to a multiple of 4 and kept inside idx)
 //           and 8 four-byte row words 256 bytes apart, and lane 0 stores the
 //           exclusive or of the 20 words it loaded.
+//   hops 4  the pooled decode's memory pattern without its arithmetic: the
+//           first hop of hops 3, except that each warp pair (a request)
+//           reads 8 rows of its own, each warp one half of each; then, for
+//           one warp pair in four (a request whose pool closes), a second hop
+//           that depends on idx[w]: 30 row words per thread from the 8 KB
+//           block holding row idx[w] (as a closing pool's 15 key and 15 score
+//           ring rows), issued before each thread stores its 8 first-hop row
+//           words (1 KB per warp, as the ring stashes of a request's tokens);
+//           lane 0 finally stores the exclusive or of all it loaded.  The
+//           grid's dependents are released after the first hop, as in the
+//           decode.
 // Every load takes the read-only path (ld.global.nc), as the decode's own
 // index and row loads do.  An index outside [0, num_rows) is skipped.
 #include <cstdint>
@@ -35,7 +46,7 @@ template <int kHops>
 __global__ void latency_probe_kernel(const int32_t* idx, const uint2* rows, int64_t num_rows, uint2* out,
                                      int32_t n_warps) {
   pdl_wait();
-  pdl_trigger();
+  if constexpr (kHops != 4) pdl_trigger();
   if constexpr (kHops > 0) {
     const int lane = threadIdx.x & 31;
     const int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -46,7 +57,7 @@ __global__ void latency_probe_kernel(const int32_t* idx, const uint2* rows, int6
     } else if constexpr (kHops == 2) {
       if (r < 0 || r >= num_rows) return;
       out[w * 32 + lane] = __ldg(rows + static_cast<int64_t>(r) * 32 + lane);
-    } else {
+    } else if constexpr (kHops == 3) {
       // n_warps >= 16 and num_rows >= 9 (checked by the caller): the 16 index
       // words and the 8 row words below stay inside idx and rows
       const int64_t b0 = min(w & ~int64_t{3}, static_cast<int64_t>(n_warps) - 16);
@@ -57,6 +68,43 @@ __global__ void latency_probe_kernel(const int32_t* idx, const uint2* rows, int6
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc ^= static_cast<int32_t>(__ldg(rw + q * 64));
       if (lane == 0) reinterpret_cast<int32_t*>(out + w * 32)[0] = acc;
+    } else {
+      // n_warps >= 16 and num_rows >= 64 (checked by the caller); out holds
+      // 1 KB per warp
+      const int64_t b0 = min(w & ~int64_t{3}, static_cast<int64_t>(n_warps) - 16);
+      int32_t acc = r;
+#pragma unroll
+      for (int q = 1; q < 12; ++q) acc ^= __ldg(idx + b0 + ((q * 7) & 15));
+      // each warp pair (a request) reads its own 2 KB: 8 rows, a half-row each warp
+      const uint32_t* rw = reinterpret_cast<const uint32_t*>(rows) + wrap((w >> 1) * 512, num_rows * 64 - 512) +
+                           (w & 1) * 32 + lane;
+      uint32_t v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = __ldg(rw + q * 64);
+      pdl_trigger();
+      const bool closing = ((w >> 1) & 3) == 0 && r >= 0 && r < num_rows;
+      uint32_t hv[30];
+      if (closing) {
+        // the 8 KB block of 32 rows holding row r (the last whole block past it)
+        const int64_t b = min(static_cast<int64_t>(r >> 5), num_rows / 32 - 1);
+        const uint32_t* blk = reinterpret_cast<const uint32_t*>(rows) + b * 2048 + (w & 1) * 32 + lane;
+#pragma unroll
+        for (int q = 0; q < 15; ++q) {
+          hv[q] = __ldg(blk + q * 64);
+          hv[15 + q] = __ldg(blk + (16 + q) * 64);
+        }
+      }
+      uint32_t* o = reinterpret_cast<uint32_t*>(out) + w * 256 + lane;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        o[q * 32] = v[q];
+        acc ^= static_cast<int32_t>(v[q]);
+      }
+      if (closing) {
+#pragma unroll
+        for (int q = 0; q < 30; ++q) acc ^= static_cast<int32_t>(hv[q]);
+      }
+      if (lane == 0) reinterpret_cast<int32_t*>(out)[w * 256] = acc;
     }
   }
 }
@@ -74,6 +122,7 @@ cudaError_t launch_latency_probe(int hops, const int32_t* idx, const void* rows,
     case 1: return launch_ex(latency_probe_kernel<1>, grid, block, 0, use_pdl, s, idx, r, num_rows, o, n_warps);
     case 2: return launch_ex(latency_probe_kernel<2>, grid, block, 0, use_pdl, s, idx, r, num_rows, o, n_warps);
     case 3: return launch_ex(latency_probe_kernel<3>, grid, block, 0, use_pdl, s, idx, r, num_rows, o, n_warps);
+    case 4: return launch_ex(latency_probe_kernel<4>, grid, block, 0, use_pdl, s, idx, r, num_rows, o, n_warps);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -463,12 +463,31 @@ ckv_status ckv_c128_online_prefill_counted_fp8(float* state, int64_t num_slots, 
  *              exclusive or of the 20 words it loaded (idx[w] among them) to
  *              the first 4 bytes of row w of out.  Needs n_warps >= 16 and
  *              num_rows >= 9.
+ *   hops == 4  the pooled decode's memory pattern without its arithmetic:
+ *              the index loads of hops == 3 and 8 row words per thread from
+ *              the warp pair's own 2 KB (starting at word ((w / 2) 512 mod
+ *              (64 num_rows - 512)) + 32 (w mod 2) + lane, 256 bytes apart:
+ *              8 rows, a half-row for each warp, as a request's 4 key and 4
+ *              score rows); then warps whose pair index (w / 2) is a multiple
+ *              of 4 (a request whose pool closes) load, if 0 <= idx[w] <
+ *              num_rows, 30 words per thread from the 8 KB block min(idx[w] /
+ *              32, num_rows / 32 - 1) of rows (32 rows each): rows 0..14 and
+ *              16..30, at word 32 (w mod 2) + lane of each (as a closing
+ *              pool's 15 key and 15 score ring rows); then each thread stores
+ *              its 8 first-hop row words to bytes [1024 w, 1024 w + 1024) of
+ *              out (word q of lane l at word 256 w + 32 q + l), as the ring
+ *              stashes of a request's tokens; lane 0 finally stores the
+ *              exclusive or of every word it loaded to the first 4 bytes of
+ *              warp w's kilobyte.  Needs n_warps >= 16 and num_rows >= 64.
  *   idx        device int32 [n_warps] (hops >= 1); an index outside
- *              [0, num_rows) makes that warp skip its row (hops == 2)
+ *              [0, num_rows) makes that warp skip its row (hops == 2) or its
+ *              second hop (hops == 4)
  *   rows       device [num_rows][256 bytes], 8-byte aligned (hops >= 2)
- *   out        device [n_warps][256 bytes], 8-byte aligned (hops >= 1)
- * Sizes outside hops 0..3, 1 <= n_warps <= 2^30, 1 <= warps_per_cta <= 32
- * (and the hops == 3 minimums) return CKV_ERR_SHAPE and launch nothing.
+ *   out        device [n_warps][256 bytes] (hops 1..3) or [4 n_warps][256
+ *              bytes] (hops == 4), 8-byte aligned
+ * Sizes outside hops 0..4, 1 <= n_warps <= 2^30, 1 <= warps_per_cta <= 32
+ * (and the hops == 3 and 4 minimums) return CKV_ERR_SHAPE and launch
+ * nothing.
  */
 ckv_status ckv_latency_probe(int32_t hops, const int32_t* idx, const void* rows, int64_t num_rows, void* out,
                              int32_t n_warps, int32_t warps_per_cta, int32_t use_pdl, void* stream);

@@ -2,8 +2,10 @@
 do the memory work they claim.  Two hops: each warp copies the row its index
 names (out of range: the warp writes nothing); one hop: each warp writes its
 index word to the first 4 bytes of its output row; the first-hop mode: lane
-0's exclusive or of the 12 index words and 8 row words it loaded; zero hops:
-nothing."""
+0's exclusive or of the 12 index words and 8 row words it loaded; the
+decode-pattern mode: the 8 row words of every lane stored to the warp's
+kilobyte, and lane 0's exclusive or of all it loaded, closing warp pairs'
+block words included; zero hops: nothing."""
 import numpy as np
 import pytest
 import torch
@@ -70,3 +72,33 @@ def test_probe_first_hop_mode(ck, n):
     o = out.cpu().numpy()
     np.testing.assert_array_equal(o[:, :4].copy().view(np.uint32)[:, 0], want)
     assert np.all(o[:, 4:] == 0xEE)
+
+
+@pytest.mark.parametrize("n,nrows", [(16, 64), (1024, 16384), (778, 100)])
+def test_probe_decode_pattern_mode(ck, n, nrows):
+    g = torch.Generator().manual_seed(n + nrows)
+    idx = torch.randint(-5, nrows + 5, (n,), generator=g, dtype=torch.int32)  # some out of range
+    rows = torch.randint(0, 256, (nrows, 256), generator=g, dtype=torch.uint8)
+    out = torch.full((4 * n, 256), 0xEE, dtype=torch.uint8, device="cuda")
+    ck.ckv_latency_probe(4, n, idx.cuda(), rows.cuda(), out, warps_per_cta=2, use_pdl=True)
+    torch.cuda.synchronize()
+    iw = idx.numpy()
+    rw = rows.numpy().view(np.uint32).reshape(-1)
+    o = out.cpu().numpy().view(np.uint32).reshape(n, 256)
+    blocks = nrows // 32
+    for w in range(n):
+        first = ((w >> 1) * 512) % (nrows * 64 - 512) + (w & 1) * 32
+        want = np.array([rw[first + q * 64 + lane] for q in range(8) for lane in range(32)], np.uint32)
+        b0 = min(w & ~3, n - 16)
+        acc = np.uint32(iw[w])
+        for q in range(1, 12):
+            acc ^= np.uint32(iw[b0 + ((q * 7) & 15)])
+        for q in range(8):
+            acc ^= rw[first + q * 64]
+        r = int(iw[w])
+        if ((w >> 1) & 3) == 0 and 0 <= r < nrows:
+            blk = min(r >> 5, blocks - 1) * 2048 + (w & 1) * 32
+            for q in list(range(15)) + list(range(16, 31)):
+                acc ^= rw[blk + q * 64]
+        want[0] = acc
+        np.testing.assert_array_equal(o[w], want)

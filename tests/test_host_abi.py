@@ -56,7 +56,9 @@ def test_validation_rejects_before_launch(lib):
     assert lib.ckv_c128_online_decode(P(20), 4, one, 0, one, one, one, one, 3, 128, 0, None, None) == 4
     assert lib.ckv_c128_online_decode(None, 4, None, 0, None, None, None, None, 0, 128, 0, None, None) == 0
     # latency probe: bad hop count, warps, null rows for two hops, misaligned out
-    assert lib.ckv_latency_probe(4, one, one, 4, one, 8, 4, 0, None) == 2
+    assert lib.ckv_latency_probe(5, one, one, 4, one, 8, 4, 0, None) == 2
+    assert lib.ckv_latency_probe(4, one, one, 4096, one, 8, 4, 0, None) == 2  # decode pattern: >= 16 warps
+    assert lib.ckv_latency_probe(4, one, one, 63, one, 64, 4, 0, None) == 2   # ... and >= 64 rows
     assert lib.ckv_latency_probe(3, one, one, 4096, one, 8, 4, 0, None) == 2  # first-hop mode: >= 16 warps
     assert lib.ckv_latency_probe(3, one, one, 8, one, 64, 4, 0, None) == 2    # ... and >= 9 rows
     assert lib.ckv_latency_probe(3, one, None, 4096, one, 64, 4, 0, None) == 1
