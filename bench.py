@@ -1183,7 +1183,8 @@ def main():
                                ("c128_online_decode", "c128_decode", True),
                                ("c128_online_decode_fp8", "c128_decode_fp8", True),
                                ("latency_floor_2hops", "latency_floor2", True),
-                               ("latency_floor_0hops", "latency_floor0", True)):
+                               ("latency_floor_0hops", "latency_floor0", True),
+                               ("latency_floor_decode_pattern", "latency_floor4_w1024_c2_r16384", True)):
             r = rotation_timings(case, round_scale=rs)
             e = {"instances": r["instances"], "bytes_per_call": r["bytes_per_call"],
                  "us_per_call_cold": r["pdl"]["us_per_call_cold"], "gbs_cold": r["pdl"]["gbs_cold"],
@@ -1200,8 +1201,9 @@ def main():
                                  "c128 decode: every state pool restored from a pristine copy and a 2 x L2 buffer "
                                  "written before each replay (outside the events); the fp8 entry stores FP8 rows "
                                  "instead of fp32 rows. latency_floor: the probe "
-                                 "kernels in the pooled decode's launch shape (512 warps, 4 per CTA), L2 flushed "
-                                 "before each replay")
+                                 "kernels (512 warps, 4 per CTA; the decode pattern: 1024 warps, 2 per CTA, the "
+                                 "pooled decode's own launch shape, over a 4 MB row buffer), L2 flushed before each "
+                                 "replay")
 
     if rank == 0:
         print(json.dumps({
